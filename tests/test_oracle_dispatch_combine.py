@@ -1,0 +1,221 @@
+"""Pins of the oracle's dispatch rows and combine reduction.
+
+Dispatch (PR #753 Approach; PR #690 review of the copy epilogue): every
+deduplicated (token, destination) entry receives the token's hidden row
+unchanged (bf16 copy), or its FP8 cast with per-128-column scales; pre-cast FP8
+rows and their scales travel verbatim; the sidecar rows carry the routing and
+the source metadata.
+
+Combine: combine(dispatch(x)) with identity experts equals the weight sum
+times x (to one bf16 ulp); a single lane with weight 1 returns x exactly;
+power-of-two weights are exact; zero expert outputs give +0.
+"""
+from types import SimpleNamespace
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+
+
+def small(name, **kw):
+    return W.PARITY[name].replace(**kw)
+
+
+def _bits(t):
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def dedup_entries(wl, idx, slot):
+    """(s, t, d, row) of every deduplicated entry: the first lane per destination."""
+    L = wl.num_experts // wl.num_ranks
+    R, T, K = idx.shape
+    out = []
+    for s in range(R):
+        for t in range(T):
+            seen = set()
+            for k in range(K):
+                e = idx[s, t, k]
+                if e < 0:
+                    continue
+                d = int(e) // L
+                if d in seen:
+                    continue
+                seen.add(d)
+                out.append((s, t, d, int(slot[s, t, k])))
+    return out
+
+
+@pytest.mark.parametrize("name", ["tiny_direct", "hybrid_rowform"])
+def test_bf16_rows_are_the_source_rows(orc, name):
+    wl = small(name, num_tokens=40, num_max_tokens_per_rank=48, hidden=256)
+    idx, w = W.routing(wl)
+    x, _ = W.hidden(wl)
+    st, lay = orc.layout(wl, idx)
+    st2, rec = orc.dispatch(wl, lay, x, None, idx, w)
+    assert st == 0 and st2 == 0
+    R, M, K = wl.num_ranks, wl.num_max_tokens_per_rank, wl.num_topk
+    L = wl.num_experts // R
+    xb = _bits(x)
+    idx = idx.numpy()
+    w = w.numpy()
+    ents = dedup_entries(wl, idx, lay["slot_map"])
+    filled = np.zeros(rec["recv_x"].shape[0], bool)
+    for s, t, d, row in ents:
+        g = d * R * M + row
+        filled[g] = True
+        assert np.array_equal(rec["recv_x"][g], xb[s, t])
+        # sidecars: destination-local expert index / weight on lanes to d, else -1 / 0
+        on = (idx[s, t] >= 0) & (idx[s, t] // L == d)
+        assert rec["recv_topk_idx"][d, row].tolist() == np.where(on, idx[s, t] - d * L, -1).tolist()
+        assert rec["recv_topk_weights"][d, row].tolist() == np.where(on, w[s, t], 0.0).astype(np.float32).tolist()
+        assert rec["recv_src_metadata"][d, row].tolist() == [s, t] + [-1] * K
+    assert not rec["recv_x"][~filled].any()
+    assert filled.sum() == lay["num_tokens_per_rank"].sum()
+
+
+def test_precast_fp8_rows_and_scales_are_verbatim(orc):
+    wl = small("dsv3_fp8_precast", num_tokens=20, num_max_tokens_per_rank=20, hidden=512)
+    idx, w = W.routing(wl)
+    x, sf = W.hidden(wl)
+    _, lay = orc.layout(wl, idx)
+    st, rec = orc.dispatch(wl, lay, x, sf, idx, w)
+    assert st == 0
+    R, M = wl.num_ranks, wl.num_max_tokens_per_rank
+    for s, t, d, row in dedup_entries(wl, idx.numpy(), lay["slot_map"]):
+        g = d * R * M + row
+        assert np.array_equal(rec["recv_x"][g], x[s, t].numpy())
+        assert np.array_equal(rec["recv_sf"][g], sf[s, t].numpy())
+
+
+def test_fused_cast_rows(orc):
+    wl = small("dsv3_fp8", num_tokens=12, num_max_tokens_per_rank=16, hidden=1152)
+    idx, w = W.routing(wl)
+    x, _ = W.hidden(wl)
+    _, lay = orc.layout(wl, idx)
+    st, rec = orc.dispatch(wl, lay, x, None, idx, w)
+    assert st == 0
+    R, M = wl.num_ranks, wl.num_max_tokens_per_rank
+    xb = _bits(x)
+    for s, t, d, row in dedup_entries(wl, idx.numpy(), lay["slot_map"]):
+        g = d * R * M + row
+        q, sf = orc.cast_row_fp8(xb[s, t])
+        assert np.array_equal(rec["recv_x"][g], q)
+        assert np.array_equal(rec["recv_sf"][g], sf)
+        # dequantised row within the e4m3 rounding bound of the source row
+        xf = orc.bf16_to_f32(xb[s, t]).astype(np.float64)
+        deq = orc.e4m3_to_f32(q).astype(np.float64) * np.repeat(sf, 128)
+        assert np.all(np.abs(deq - xf) <= (2 ** -4 + 1e-6) * np.abs(xf) + 2 ** -10 * np.repeat(sf, 128) * 1.0001)
+
+
+def test_expanded_rows_and_metadata(orc):
+    wl = small("expanded", num_tokens=24, num_max_tokens_per_rank=24, hidden=256, expert_alignment=4)
+    idx, w = W.routing(wl)
+    x, _ = W.hidden(wl)
+    st, lay = orc.layout(wl, idx)
+    st2, rec = orc.dispatch(wl, lay, x, None, idx, w)
+    assert st == 0 and st2 == 0
+    R, M, K = wl.num_ranks, wl.num_max_tokens_per_rank, wl.num_topk
+    L = wl.num_experts // R
+    xb = _bits(x)
+    idx = idx.numpy()
+    pos, region = lay["exp_pos"], lay["exp_region"]
+    n = 0
+    for s in range(R):
+        for t in range(wl.num_tokens):
+            for k in range(K):
+                e = idx[s, t, k]
+                if e < 0:
+                    continue
+                d = e // L
+                assert np.array_equal(rec["recv_x"][region[d] + pos[s, t, k]], xb[s, t])
+                n += 1
+    assert n == int(lay["exp_cnt"].sum())
+    for s, t, d, row in dedup_entries(wl, idx, lay["slot_map"]):
+        on = (idx[s, t] >= 0) & (idx[s, t] // L == d)
+        assert rec["recv_src_metadata"][d, row].tolist() == [s, t] + np.where(on, pos[s, t], -1).tolist()
+
+
+# ---- combine -------------------------------------------------------------
+
+def _ulp_bf16(v):
+    """bf16 spacing at |v| (binary64)."""
+    v = np.abs(v)
+    e = np.floor(np.log2(np.where(v > 0, v, 1.0)))
+    return np.where(v > 0, 2.0 ** (e - 7), 2.0 ** -133)
+
+
+@pytest.mark.parametrize("name", ["tiny_direct", "hybrid_rowform", "expanded"])
+def test_identity_experts_give_weight_sum_times_x(orc, name):
+    wl = small(name, num_tokens=30, num_max_tokens_per_rank=32, hidden=256)
+    idx, w = W.routing(wl)
+    x, _ = W.hidden(wl)
+    _, lay = orc.layout(wl, idx)
+    _, rec = orc.dispatch(wl, lay, x, None, idx, w)
+    st, out = orc.combine(wl, lay, rec["recv_x"], idx, w)
+    assert st == 0
+    xf = orc.bf16_to_f32(_bits(x)).astype(np.float64)
+    wsum = np.where(idx.numpy() >= 0, w.numpy().astype(np.float64), 0).sum(-1)
+    closed = wsum[..., None] * xf
+    got = orc.bf16_to_f32(out).astype(np.float64)
+    assert np.all(np.abs(got - closed) <= _ulp_bf16(closed))
+
+
+def test_single_lane_unit_weight_returns_x(orc):
+    wl = small("tiny_direct", num_topk=1, num_tokens=50, num_max_tokens_per_rank=50, hidden=384)
+    idx, _ = W.routing(wl)
+    w = torch.ones_like(idx, dtype=torch.float32)
+    x, _ = W.hidden(wl)
+    _, lay = orc.layout(wl, idx)
+    _, rec = orc.dispatch(wl, lay, x, None, idx, w)
+    _, out = orc.combine(wl, lay, rec["recv_x"], idx, w)
+    assert np.array_equal(out, _bits(x))
+
+
+def test_power_of_two_weights_are_exact(orc):
+    wl = small("direct_zipf", num_tokens=25, num_max_tokens_per_rank=25, hidden=256)
+    idx, _ = W.routing(wl)
+    K = wl.num_topk
+    w = torch.tensor([2.0 ** -(k + 1) for k in range(K)], dtype=torch.float32).expand_as(idx).contiguous()
+    w = w.masked_fill(idx < 0, 0.0)
+    x, _ = W.hidden(wl)
+    _, lay = orc.layout(wl, idx)
+    _, rec = orc.dispatch(wl, lay, x, None, idx, w)
+    _, out = orc.combine(wl, lay, rec["recv_x"], idx, w)
+    # bf16 x has 8 significant bits; the weighted sum spans < 24 bits: exact in fp32
+    exact = (w.double().sum(-1, keepdim=True) * x.double()).float()
+    assert np.array_equal(out, _bits(exact.to(torch.bfloat16)))
+
+
+def test_zero_outputs_give_positive_zero(orc):
+    wl = small("direct_zipf", num_tokens=10, num_max_tokens_per_rank=10, hidden=128)
+    idx, w = W.routing(wl)
+    _, lay = orc.layout(wl, idx)
+    y = np.zeros((orc.recv_rows(wl), wl.hidden), np.uint16)
+    _, out = orc.combine(wl, lay, y, idx, w)
+    assert np.all(out == 0)  # +0, never -0
+
+
+def test_combine_token_hand_worked(orc):
+    one, three = orc.f32_to_bf16(np.array([1.0, 3.0], np.float32))
+    rows = [np.full(4, one, np.uint16), None, np.full(4, three, np.uint16)]
+    out = orc.combine_token(rows, np.array([0.5, 7.0, 0.25], np.float32))
+    # 0.5*1 + 0.25*3 = 1.25 (the masked lane's weight is ignored) -> bf16 0x3FA0
+    assert out.tolist() == [0x3FA0] * 4
+    assert orc.combine_token([None, None], np.array([1.0, 1.0], np.float32)).size == 0
+
+
+def test_combine_is_a_fused_chain_in_lane_order(orc):
+    # y = [1, 1, 2^-24], w = [1, 2^-8, 1 + 2^-23]. In lane order with fused
+    # multiply-adds: acc = 1, then 1 + 2^-8 (exact), then the exact sum
+    # 1 + 2^-8 + 2^-24 + 2^-47 rounds up to 1 + 2^-8 + 2^-23 in binary32, which is
+    # above the bf16 tie at 1 + 2^-8, so the result is 1 + 2^-7 (0x3F81).
+    # Rounding the last product first (2^-24), or summing in reverse lane order,
+    # lands exactly on the tie instead and gives 1.0 (0x3F80).
+    y = orc.f32_to_bf16(np.array([1.0, 1.0, 2.0 ** -24], np.float32))
+    w = np.array([1.0, 2.0 ** -8, 1 + 2.0 ** -23], np.float32)
+    out = orc.combine_token([np.array([v], np.uint16) for v in y], w)
+    assert out.tolist() == [0x3F81]
+    rev = orc.combine_token([np.array([v], np.uint16) for v in y[::-1]], w[::-1].copy())
+    assert rev.tolist() == [0x3F80]
