@@ -1,0 +1,477 @@
+"""Benchmark of one MoE dispatch + combine step on one GPU (N replicas under torchrun).
+
+A step is the whole hot path over one batch of synthetic input already resident
+in device memory: the dispatch layout (count, scan, slots), the dispatch
+scatter (with the fused bf16 -> FP8-e4m3 cast on the DeepSeek-V3-shaped
+workload) and the weighted combine. The metric is tokens/s (source tokens of
+all logical ranks per second) and the HBM bandwidth each phase achieves.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the CPU oracle, timed on the host
+
+Prints one JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "dispatch+combine tokens/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
+DEFAULT_WORKLOAD = "dsv3_fp8"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="native", choices=["native", "reference"])
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
+    p.add_argument("--tokens", type=int, default=0,
+                   help="override tokens per rank (small cases for profiling only)")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline sample")
+    return p.parse_args()
+
+
+def workload(args):
+    wl = W.WORKLOADS[args.workload]
+    if args.tokens:
+        wl = wl.replace(num_tokens=args.tokens, num_max_tokens_per_rank=max(args.tokens, 1))
+    return wl
+
+
+def describe(wl) -> str:
+    lay = "expanded per-expert blocks" if wl.expand else (
+        f"hybrid row form {wl.n_so}x{wl.n_su}" if wl.n_so > 1 else "direct row form")
+    cast = {("bf16", "fp8"): "bf16 x cast to fp8-e4m3 inside dispatch (fp32 scale per 128 columns)",
+            ("fp8", "fp8"): "pre-cast fp8-e4m3 x + fp32 scales",
+            ("bf16", "bf16"): "bf16 rows"}[(wl.x_dtype, wl.recv_dtype)]
+    return (f"{wl.name}: {wl.num_ranks} logical ranks x {wl.num_tokens} tokens, {wl.num_experts} experts "
+            f"top-{wl.num_topk}, hidden {wl.hidden}, {lay}, {cast}, bf16 combine with fp32 weights, "
+            f"routing {wl.routing}")
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---- algorithmic bytes (only what the method must move) ---------------------
+
+def algorithmic_bytes(wl, ntpr, valid_lanes, tokens_with_lane):
+    """Bytes per launch of each phase. ntpr: total deduplicated rows; valid_lanes:
+    lanes with an expert; tokens_with_lane: source tokens with >= 1 valid lane."""
+    R, T, K, H = wl.num_ranks, wl.num_tokens, wl.num_topk, wl.hidden
+    G = H // 128
+    n_tok = R * T
+    eb_in = 1 if wl.x_dtype == "fp8" else 2
+    eb_out = 1 if wl.recv_dtype == "fp8" else 2
+    hid_rows = valid_lanes if wl.expand else ntpr
+    layout = n_tok * K * 8 + n_tok * K * 4 + n_tok * R + 4 * R * (R + wl.num_experts) * 2
+    if wl.expand:
+        layout += n_tok * K * 4
+    dispatch = (tokens_with_lane * H * eb_in                       # x read once per routed token
+                + (tokens_with_lane * G * 4 if wl.x_dtype == "fp8" else 0)
+                + hid_rows * H * eb_out                            # hidden rows written
+                + (hid_rows * G * 4 if wl.recv_dtype == "fp8" else 0)
+                + ntpr * (K * 8 + K * 4 + (2 + K) * 4)             # sidecar rows
+                + n_tok * K * (8 + 4 + 4))                         # topk_idx, weights, slots read
+    combine = (hid_rows * H * 2                                    # each expert-output row once
+               + n_tok * H * 2                                     # out written
+               + n_tok * K * (8 + 4 + 4))
+    return {"layout": layout, "dispatch": dispatch, "combine": combine}
+
+
+# ---- clocks ----------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.25)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---- the native arm ---------------------------------------------------------
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, v):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def native(args):
+    import combine_ep_get_02_gb300 as ep
+
+    world, rank, local = dist_setup(args)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = workload(args)
+    cfg = ep.config_of(wl)
+    R, T, K, H = wl.num_ranks, wl.num_tokens, wl.num_topk, wl.hidden
+
+    # inputs: seeded, generated on the host, then resident in device memory
+    idx_h, w_h = W.routing(wl)
+    x_h, sf_h = W.hidden(wl)
+    idx, w, x = idx_h.to(dev), w_h.to(dev), x_h.to(dev)
+    sf = None if sf_h is None else sf_h.to(dev)
+    ws = ep.alloc_workspace(cfg, dev)
+    lay = ep.alloc_layout(cfg, dev)
+    recv = ep.alloc_recv(cfg, dev)
+    rows = ep.ep_recv_rows(cfg)
+    identity = wl.y_kind == "identity" and wl.recv_dtype == "bf16"
+    y = recv.recv_x if identity else W.expert_outputs(wl, rows, device=str(dev))
+    out = torch.empty(R, T, H, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+
+    def step(e=None):
+        if e: e[0].record(stream)
+        ep.ep_get_dispatch_layout(cfg, idx, lay, ws, stream)
+        if e: e[1].record(stream)
+        ep.ep_dispatch(cfg, lay, x, sf, idx, w, recv, ws, stream)
+        if e: e[2].record(stream)
+        ep.ep_combine(cfg, lay, y, idx, w, out, ws, stream)
+        if e: e[3].record(stream)
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize(dev)
+    st = ep.ep_check_error(ws, stream)
+    if st != ep.EP_OK:
+        raise RuntimeError(f"device status {ep.ep_status_string(st)}")
+
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(ev[i])
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+    total_ms = t_start.elapsed_time(t_end)
+    total_ms = max_over_ranks(world, total_ms)
+    ms_per_step = total_ms / args.steps
+    phase_ms = {name: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev)
+                for j, name in enumerate(("layout", "dispatch", "combine"))}
+
+    # algorithmic bytes from this layout's counts
+    ntpr = int(lay.num_tokens_per_rank.sum().item())
+    valid = idx_h >= 0
+    valid_lanes = int(valid.sum().item())
+    tokens_with_lane = int(valid.any(-1).sum().item())
+    abytes = algorithmic_bytes(wl, ntpr, valid_lanes, tokens_with_lane)
+    peak, peak_kind = peaks()
+    gbs = {k: abytes[k] / (phase_ms[k] * 1e-3) / 1e9 for k in abytes}
+    dominant = max(("dispatch", "combine"), key=lambda k: phase_ms[k])
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = end_to_end(ep, cfg, wl, idx_h, w_h, x_h, sf_h, lay, recv, y, identity, ws, stream, dev,
+                         args, world)
+
+    n_units = world * R * T
+    line = {
+        "metric": METRIC,
+        "value": n_units / (total_ms * 1e-3 / args.steps),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": ("bf16 x -> fp8-e4m3 recv, fp32 combine accumulate"
+                  if wl.recv_dtype == "fp8" and wl.x_dtype == "bf16" else
+                  f"{wl.x_dtype} x -> {wl.recv_dtype} recv, fp32 combine accumulate"),
+        "data": "synthetic (seeded routing and activations)",
+        "config": {"workload": describe(wl), "tokens_per_step": R * T, "dedup_rows": ntpr,
+                   "l2": "inputs larger than L2 between steps (no flush)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "phases": {
+            k: {"us": phase_ms[k] * 1e3, "algorithmic_bytes": abytes[k], "gbs": gbs[k],
+                "frac_of_peak": gbs[k] / peak} for k in ("layout", "dispatch", "combine")},
+        "roofline": {"kernel": f"{dominant}_kernel", "bound": "hbm", "achieved": gbs[dominant],
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": gbs[dominant] / peak, "traffic": ncu_traffic(dominant, wl, R * T)},
+        "clocks": clocks.summary(),
+        "gpu_launches": args.steps * (5 if T > 0 else 1),
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, idx_h, w_h, x_h, sf_h, y, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def end_to_end(ep, cfg, wl, idx_h, w_h, x_h, sf_h, lay, recv, y, identity, ws, stream, dev, args,
+               world):
+    """The same step through the public API from pinned host buffers: host->device
+    copies of the step's inputs and the device->host copy of its output are inside
+    the timed region."""
+    R, T, H = wl.num_ranks, wl.num_tokens, wl.hidden
+    hx = x_h.pin_memory()
+    hidx = idx_h.pin_memory()
+    hw = w_h.pin_memory()
+    hsf = None if sf_h is None else sf_h.pin_memory()
+    hout = torch.empty(R, T, H, dtype=torch.bfloat16).pin_memory()
+    dx = torch.empty_like(hx, device=dev)
+    didx = torch.empty_like(hidx, device=dev)
+    dw = torch.empty_like(hw, device=dev)
+    dsf = None if hsf is None else torch.empty_like(hsf, device=dev)
+    dout = torch.empty(R, T, H, dtype=torch.bfloat16, device=dev)
+    steps = max(3, min(args.steps, 10))
+
+    def step():
+        dx.copy_(hx, non_blocking=True)
+        didx.copy_(hidx, non_blocking=True)
+        dw.copy_(hw, non_blocking=True)
+        if dsf is not None:
+            dsf.copy_(hsf, non_blocking=True)
+        ep.ep_get_dispatch_layout(cfg, didx, lay, ws, stream)
+        ep.ep_dispatch(cfg, lay, dx, dsf, didx, dw, recv, ws, stream)
+        ep.ep_combine(cfg, lay, recv.recv_x if identity else y, didx, dw, dout, ws, stream)
+        hout.copy_(dout, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(world, a.elapsed_time(b)) / steps
+    h2d = hx.numel() * hx.element_size() + hidx.numel() * 8 + hw.numel() * 4 + \
+        (0 if hsf is None else hsf.numel() * 4)
+    d2h = hout.numel() * 2
+    return {"value": world * R * T / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def ncu_traffic(kernel, wl, n_tok):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it was
+    taken on the current kernel source; scaled by source tokens when the capture
+    ran a smaller case. None when there is no matching capture."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    try:
+        from combine_ep_get_02_gb300 import _build
+        import hashlib
+        h = hashlib.sha256()
+        for p in _build.sources():
+            h.update(open(p, "rb").read())
+        src = h.hexdigest()[:16]
+        for line in open(path):
+            f = line.split()
+            if len(f) == 6 and f[0] == kernel and f[1] == wl.name and f[5] == src:
+                bytes_, tokens = float(f[2]) + float(f[3]), float(f[4])
+                return bytes_ * n_tok / tokens
+    except Exception:
+        return None
+    return None
+
+
+# ---- the CPU oracle (baseline leg and reference arm) --------------------------
+
+def cpu_sample(wl, idx_h, w_h, x_h, sf_h, y_dev, n_tokens, seed=0):
+    """Oracle time per source token over a bounded sample: the layout of the whole
+    input (its cost spread over all tokens) + dispatch and combine of n_tokens
+    tokens drawn with a seeded generator."""
+    import oracle
+    R, T, K = wl.num_ranks, wl.num_tokens, wl.num_topk
+    t0 = time.perf_counter()
+    st, olay = oracle.layout(wl, idx_h)
+    t_layout = time.perf_counter() - t0
+    rng = np.random.default_rng(seed)
+    toks = rng.choice(R * T, size=min(n_tokens, R * T), replace=False)
+    idx_np = idx_h.numpy().reshape(R * T, K)
+    w_np = w_h.numpy().reshape(R * T, K)
+    xv = x_h.reshape(R * T, -1)
+    xv = xv.view(torch.int16).numpy().view(np.uint16) if xv.dtype == torch.bfloat16 else xv.numpy()
+    sfv = None if sf_h is None else sf_h.reshape(R * T, -1).numpy()
+    lane_rows = oracle.global_rows(wl, olay, idx_h).reshape(R * T, K)[toks]
+    uniq, inv = np.unique(lane_rows[lane_rows >= 0], return_inverse=True)
+    compact = np.full(lane_rows.shape, -1, np.int64)
+    compact[lane_rows >= 0] = inv
+    ys = y_dev.index_select(0, torch.from_numpy(uniq).to(y_dev.device)).cpu()
+    ys = ys.view(torch.int16).numpy().view(np.uint16)
+    t0 = time.perf_counter()
+    for tok in toks:
+        s, t = divmod(int(tok), T)
+        oracle.dispatch_token(wl, olay, s, t, xv[tok], None if sfv is None else sfv[tok],
+                              idx_np[tok], w_np[tok])
+    t_disp = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    oracle.combine_gathered(compact, ys, w_np[toks])
+    t_comb = time.perf_counter() - t0
+    per_token = t_layout / (R * T) + (t_disp + t_comb) / len(toks)
+    return per_token, len(toks), t_layout, t_disp, t_comb
+
+
+def cpu_baseline(wl, idx_h, w_h, x_h, sf_h, y_dev, seconds):
+    # calibrate the sample so the whole measurement takes about `seconds`
+    per, n, *_ = cpu_sample(wl, idx_h, w_h, x_h, sf_h, y_dev, 64, seed=1)
+    n = int(max(64, min(wl.num_ranks * wl.num_tokens, seconds / per)))
+    per, n, tl, td, tc = cpu_sample(wl, idx_h, w_h, x_h, sf_h, y_dev, n)
+    return {"value": 1.0 / per, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": (f"full layout of {wl.num_ranks * wl.num_tokens} tokens ({tl:.2f} s) + dispatch "
+                       f"and combine of {n} seeded random source tokens ({td:.1f} s + {tc:.1f} s), "
+                       f"single-threaded C++ oracle, scaled to tokens/s")}
+
+
+def reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    wl = workload(args)
+    idx_h, w_h = W.routing(wl)
+    x_h, sf_h = W.hidden(wl)
+    R, T = wl.num_ranks, wl.num_tokens
+    # expert outputs for the sampled tokens: drawn on the host for the rows they read
+    import oracle
+    st, olay = oracle.layout(wl, idx_h)
+    rows = oracle.global_rows(wl, olay, idx_h)
+    n_rows = int(rows.max()) + 1 if rows.size and rows.max() >= 0 else 1
+    gen = torch.Generator().manual_seed(wl.seed * 1_000_003 + 1)
+
+    class _LazyRows:  # y rows on demand: same shape of access as a device buffer
+        device = "cpu"
+
+        def index_select(self, dim, ix):
+            return torch.randn(ix.numel(), wl.hidden, generator=gen).to(torch.bfloat16)
+
+    per_step_tokens = 256
+    times = []
+    for i in range(args.warmup + args.steps):
+        per, n, *_ = cpu_sample(wl, idx_h, w_h, x_h, sf_h, _LazyRows(), per_step_tokens, seed=i)
+        if i >= args.warmup:
+            times.append(per)
+    per = statistics.mean(times)
+    value = 1.0 / per
+    sample = (f"per step: full layout of {R * T} tokens + dispatch and combine of {per_step_tokens} "
+              f"seeded random source tokens of {describe(wl)}; single-threaded C++ oracle")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": per * R * T * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp32 oracle arithmetic", "data": "synthetic",
+            "config": {"workload": describe(wl)},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        reference(args)
+    else:
+        native(args)
+
+
+if __name__ == "__main__":
+    main()

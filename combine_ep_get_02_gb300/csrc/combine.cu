@@ -1,0 +1,124 @@
+// Combine: gather each source token's expert-output rows and reduce them with
+// the token's top-k weights.
+//
+// out[s][t] = bf16_rn(acc), acc = +0, then for k in lane order over the valid
+// lanes acc = fma(w_k, y[row of lane k], acc) in fp32. The order of the fused
+// multiply-adds is fixed, so the result is bitwise reproducible and equal to
+// the sequential definition. One warp owns one token; each lane owns 8
+// columns (one 16-byte chunk) per step and keeps the loads of all K rows of
+// two steps in flight before it reduces.
+#include "ep_device.cuh"
+#include "ep_internal.cuh"
+
+namespace ep {
+
+namespace {
+
+constexpr int kWarps = kCopyThreads / 32;
+
+template <bool kExpand, int kMaxK, int kSteps>
+__global__ void __launch_bounds__(kCopyThreads) combine_kernel(CombineArgs a) {
+  __shared__ const uint16_t* s_ptr[kWarps][kMaxK];
+  __shared__ float s_w[kWarps][kMaxK];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t gwarp = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
+  const int nchunk = a.H >> 3;  // 8 bf16 per chunk
+
+  for (int64_t tok = gwarp; tok < a.num_tokens; tok += nwarps) {
+    if (lane < kMaxK) {
+      const uint16_t* p = nullptr;
+      float w = 0.f;
+      if (lane < a.K) {
+        const int64_t i = tok * a.K + lane;
+        const int64_t e = a.topk_idx[i];
+        const int r = kExpand ? a.exp_pos[i] : a.slot_map[i];
+        if (e >= 0 && e < a.E && r >= 0) {
+          const int d = static_cast<int>(e) / a.L;
+          const int64_t row = kExpand ? static_cast<int64_t>(a.exp_region[d]) + r
+                                      : static_cast<int64_t>(d) * a.region_rows + r;
+          p = a.y + row * a.H;
+          w = a.topk_w[i];
+        }
+      }
+      s_ptr[warp][lane] = p;
+      s_w[warp][lane] = w;
+    }
+    __syncwarp();
+    const uint16_t* ptr[kMaxK];
+    float wk[kMaxK];
+#pragma unroll
+    for (int k = 0; k < kMaxK; ++k) {
+      ptr[k] = s_ptr[warp][k];
+      wk[k] = s_w[warp][k];
+    }
+    uint16_t* orow = a.out + tok * a.H;
+    for (int c0 = lane; c0 < nchunk; c0 += 32 * kSteps) {
+      uint4 v[kSteps][kMaxK];
+#pragma unroll
+      for (int h = 0; h < kSteps; ++h) {
+        const int c = c0 + h * 32;
+#pragma unroll
+        for (int k = 0; k < kMaxK; ++k)
+          if (ptr[k] != nullptr && c < nchunk) v[h][k] = ld_ro16(ptr[k] + (static_cast<size_t>(c) << 3));
+      }
+#pragma unroll
+      for (int h = 0; h < kSteps; ++h) {
+        const int c = c0 + h * 32;
+        if (c >= nchunk) continue;
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll
+        for (int k = 0; k < kMaxK; ++k) {
+          if (ptr[k] == nullptr) continue;
+          const uint32_t wv[4] = {v[h][k].x, v[h][k].y, v[h][k].z, v[h][k].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 f = bf16x2_to_f32x2(wv[i]);
+            acc[2 * i] = __fmaf_rn(wk[k], f.x, acc[2 * i]);
+            acc[2 * i + 1] = __fmaf_rn(wk[k], f.y, acc[2 * i + 1]);
+          }
+        }
+        uint4 o;
+        o.x = f32x2_to_bf16x2(acc[0], acc[1]);
+        o.y = f32x2_to_bf16x2(acc[2], acc[3]);
+        o.z = f32x2_to_bf16x2(acc[4], acc[5]);
+        o.w = f32x2_to_bf16x2(acc[6], acc[7]);
+        st16(orow + (static_cast<size_t>(c) << 3), o);
+      }
+    }
+    __syncwarp();  // s_ptr / s_w are rewritten by the next token
+  }
+}
+
+template <bool kExpand, int kMaxK, int kSteps>
+cudaError_t launch_one(const CombineArgs& a, int num_sms, cudaStream_t stream) {
+  auto kern = combine_kernel<kExpand, kMaxK, kSteps>;
+  int per_sm = 0;
+  cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kCopyThreads, 0);
+  if (err != cudaSuccess) return err;
+  if (per_sm < 1) per_sm = 1;
+  int64_t ctas = static_cast<int64_t>(num_sms) * per_sm;
+  const int64_t need = (a.num_tokens + kWarps - 1) / kWarps;
+  if (ctas > need) ctas = need;
+  if (ctas < 1) return cudaSuccess;
+  kern<<<static_cast<unsigned>(ctas), kCopyThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const Geometry& g, const CombineArgs& a, int num_sms,
+                           cudaStream_t stream) {
+  if (g.K <= 8)
+    return g.expand ? launch_one<true, 8, 2>(a, num_sms, stream)
+                    : launch_one<false, 8, 2>(a, num_sms, stream);
+  if (g.K <= 16)
+    return g.expand ? launch_one<true, 16, 1>(a, num_sms, stream)
+                    : launch_one<false, 16, 1>(a, num_sms, stream);
+  return g.expand ? launch_one<true, 32, 1>(a, num_sms, stream)
+                  : launch_one<false, 32, 1>(a, num_sms, stream);
+}
+
+}  // namespace ep

@@ -1,0 +1,218 @@
+// Dispatch: scatter every source token's hidden row into the receive rows of
+// its deduplicated destinations, with the row's sidecars.
+//
+// One warp owns one source token at a time: it reads the row once (16-byte
+// loads, each lane a strided set of chunks), optionally casts it to FP8-e4m3
+// in registers, and stores it to each destination row; the slots come from the
+// layout (PR #753, Approach: the kernel replays precomputed slots instead of
+// racing for them). Tokens are spread over a persistent grid sized to the SMs.
+// Lanes 0..K-1 carry the token's top-k lanes and write the small sidecar rows
+// (routing of the lanes to that destination and the source metadata).
+#include "ep_device.cuh"
+#include "ep_internal.cuh"
+
+namespace ep {
+
+namespace {
+
+constexpr int kWarps = kCopyThreads / 32;
+constexpr int kUnroll = 4;  // 16-byte chunks in flight per lane
+
+enum Kind { kCopyRow = 0, kCastRow = 1 };
+
+struct TokenLanes {
+  int e, d, slot, pos;
+  float w;
+  unsigned vmask;  // valid lanes
+  unsigned rmask;  // first lane per destination (deduplicated entries)
+};
+
+// Lane k < K: the token's k-th top-k lane. Invalid lanes get a distinct
+// negative d so that they never group with anything.
+__device__ __forceinline__ TokenLanes load_lanes(const DispatchArgs& a, int64_t tok, int lane,
+                                                 bool expand) {
+  TokenLanes L;
+  L.e = -1;
+  L.slot = -1;
+  L.pos = -1;
+  L.w = 0.f;
+  if (lane < a.K) {
+    const int64_t i = tok * a.K + lane;
+    const int64_t e = a.topk_idx[i];
+    L.slot = a.slot_map[i];
+    L.w = a.topk_w[i];
+    if (expand) L.pos = a.exp_pos[i];
+    L.e = (e >= 0 && e < a.E) ? static_cast<int>(e) : -1;
+  }
+  const bool valid = L.e >= 0 && (expand ? L.pos >= 0 : L.slot >= 0);
+  L.d = valid ? L.e / a.L : -1 - lane;
+  const unsigned same = __match_any_sync(kFullMask, L.d);
+  L.vmask = __ballot_sync(kFullMask, valid);
+  L.rmask = __ballot_sync(kFullMask, valid && (same & lanemask_lt()) == 0);
+  return L;
+}
+
+template <int kKind, bool kExpand>
+__global__ void __launch_bounds__(kCopyThreads) dispatch_kernel(DispatchArgs a) {
+  __shared__ int64_t s_row[kWarps][kMaxTopk];               // hidden destination rows
+  __shared__ float s_sf[kWarps][kMaxScaleGroups];           // this token's FP8 scales
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const unsigned lt = lanemask_lt();
+  const int64_t gwarp = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
+
+  for (int64_t tok = gwarp; tok < a.num_tokens; tok += nwarps) {
+    const int s = static_cast<int>(tok / a.T);
+    const int t = static_cast<int>(tok - static_cast<int64_t>(s) * a.T);
+    const TokenLanes ln = load_lanes(a, tok, lane, kExpand);
+    const unsigned hmask = kExpand ? ln.vmask : ln.rmask;
+    if ((hmask >> lane) & 1) {
+      const int64_t row = kExpand ? static_cast<int64_t>(a.exp_region[ln.d]) + ln.pos
+                                  : static_cast<int64_t>(ln.d) * a.region_rows + ln.slot;
+      s_row[warp][__popc(hmask & lt)] = row;
+    }
+    __syncwarp();
+    const int nh = __popc(hmask);
+
+    if (kKind == kCopyRow) {
+      // the row's bytes unchanged (bf16 -> bf16, or pre-cast e4m3 -> e4m3)
+      const uint8_t* src = a.x + tok * a.in_row_bytes;
+      const int nchunk = a.in_row_bytes >> 4;
+      for (int c0 = 0; c0 < nchunk; c0 += 32 * kUnroll) {
+        uint4 v[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          const int c = c0 + u * 32 + lane;
+          if (c < nchunk) v[u] = ld_stream16(src + (static_cast<size_t>(c) << 4));
+        }
+        for (int j = 0; j < nh; ++j) {
+          uint8_t* dst = a.recv_x + s_row[warp][j] * a.out_row_bytes;
+#pragma unroll
+          for (int u = 0; u < kUnroll; ++u) {
+            const int c = c0 + u * 32 + lane;
+            if (c < nchunk) st16(dst + (static_cast<size_t>(c) << 4), v[u]);
+          }
+        }
+      }
+      if (a.x_sf != nullptr) {  // pre-cast FP8: the scales travel verbatim
+        const float* ssrc = a.x_sf + tok * a.G;
+        for (int g = lane; g < a.G; g += 32) {
+          const float v = ssrc[g];
+          for (int j = 0; j < nh; ++j) a.recv_sf[s_row[warp][j] * a.G + g] = v;
+        }
+      }
+    } else {
+      // bf16 -> e4m3 with one fp32 scale per 128 columns. A lane owns 16 columns
+      // (32 bytes in, 16 bytes out); 8 consecutive lanes form one 128-column group.
+      const uint8_t* src = a.x + tok * a.in_row_bytes;
+      const int nunit = a.H >> 4;  // multiple of 8
+      for (int u0 = 0; u0 < nunit; u0 += 32 * 2) {
+        uint4 lo[2], hi[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int u = u0 + r * 32 + lane;
+          if (u < nunit) {
+            lo[r] = ld_stream16(src + (static_cast<size_t>(u) << 5));
+            hi[r] = ld_stream16(src + (static_cast<size_t>(u) << 5) + 16);
+          }
+        }
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int u = u0 + r * 32 + lane;
+          if (u0 + r * 32 >= nunit) continue;  // warp-uniform
+          float f[16];
+          const uint32_t wv[8] = {lo[r].x, lo[r].y, lo[r].z, lo[r].w, hi[r].x, hi[r].y, hi[r].z, hi[r].w};
+          float amax = 0.f;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float2 p = bf16x2_to_f32x2(u < nunit ? wv[i] : 0u);
+            f[2 * i] = p.x;
+            f[2 * i + 1] = p.y;
+            amax = fmaxf(amax, fmaxf(fabsf(p.x), fabsf(p.y)));
+          }
+          amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
+          amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 2));
+          amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 4));
+          amax = fmaxf(amax, 1e-4f);
+          const float inv = __fdiv_rn(448.0f, amax);
+          uint4 q;
+          q.x = f32x2_to_e4m3x2(__fmul_rn(f[0], inv), __fmul_rn(f[1], inv)) |
+                f32x2_to_e4m3x2(__fmul_rn(f[2], inv), __fmul_rn(f[3], inv)) << 16;
+          q.y = f32x2_to_e4m3x2(__fmul_rn(f[4], inv), __fmul_rn(f[5], inv)) |
+                f32x2_to_e4m3x2(__fmul_rn(f[6], inv), __fmul_rn(f[7], inv)) << 16;
+          q.z = f32x2_to_e4m3x2(__fmul_rn(f[8], inv), __fmul_rn(f[9], inv)) |
+                f32x2_to_e4m3x2(__fmul_rn(f[10], inv), __fmul_rn(f[11], inv)) << 16;
+          q.w = f32x2_to_e4m3x2(__fmul_rn(f[12], inv), __fmul_rn(f[13], inv)) |
+                f32x2_to_e4m3x2(__fmul_rn(f[14], inv), __fmul_rn(f[15], inv)) << 16;
+          if (u < nunit) {
+            if ((lane & 7) == 0) s_sf[warp][u >> 3] = __fdiv_rn(amax, 448.0f);
+            for (int j = 0; j < nh; ++j)
+              st16(a.recv_x + s_row[warp][j] * a.out_row_bytes + (static_cast<size_t>(u) << 4), q);
+          }
+        }
+      }
+      __syncwarp();
+      for (int g = lane; g < a.G; g += 32) {
+        const float v = s_sf[warp][g];
+        for (int j = 0; j < nh; ++j) a.recv_sf[s_row[warp][j] * a.G + g] = v;
+      }
+    }
+
+    // sidecar rows of each deduplicated destination (row form)
+    if (a.recv_idx != nullptr || a.recv_w != nullptr || a.recv_md != nullptr) {
+      const int md_d = __shfl_up_sync(kFullMask, ln.d, 2);    // lane l: lane l-2's d
+      const int md_pos = __shfl_up_sync(kFullMask, ln.pos, 2);
+      unsigned m = ln.rmask;
+      while (m) {
+        const int rl = __ffs(m) - 1;
+        m &= m - 1;
+        const int dj = __shfl_sync(kFullMask, ln.d, rl);
+        const int slot = __shfl_sync(kFullMask, ln.slot, rl);
+        const int64_t mrow = static_cast<int64_t>(dj) * a.region_rows + slot;
+        if (lane < a.K) {
+          const bool on = ln.d == dj;
+          if (a.recv_idx) a.recv_idx[mrow * a.K + lane] = on ? static_cast<int64_t>(ln.e - dj * a.L) : -1;
+          if (a.recv_w) a.recv_w[mrow * a.K + lane] = on ? ln.w : 0.f;
+        }
+        if (a.recv_md && lane < a.K + 2) {
+          int v;
+          if (lane == 0) v = s;
+          else if (lane == 1) v = t;
+          else v = (kExpand && md_d == dj) ? md_pos : -1;
+          a.recv_md[mrow * (a.K + 2) + lane] = v;
+        }
+      }
+    }
+    __syncwarp();  // s_row / s_sf are rewritten by the next token
+  }
+}
+
+template <int kKind, bool kExpand>
+cudaError_t launch_one(const DispatchArgs& a, int num_sms, cudaStream_t stream) {
+  auto kern = dispatch_kernel<kKind, kExpand>;
+  int per_sm = 0;
+  cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kCopyThreads, 0);
+  if (err != cudaSuccess) return err;
+  if (per_sm < 1) per_sm = 1;
+  int64_t ctas = static_cast<int64_t>(num_sms) * per_sm;
+  const int64_t need = (a.num_tokens + kWarps - 1) / kWarps;
+  if (ctas > need) ctas = need;
+  if (ctas < 1) return cudaSuccess;
+  kern<<<static_cast<unsigned>(ctas), kCopyThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch(const Geometry& g, const DispatchArgs& a, int num_sms,
+                            cudaStream_t stream) {
+  const bool cast = !g.x_fp8 && g.recv_fp8;
+  if (cast) {
+    return g.expand ? launch_one<kCastRow, true>(a, num_sms, stream)
+                    : launch_one<kCastRow, false>(a, num_sms, stream);
+  }
+  return g.expand ? launch_one<kCopyRow, true>(a, num_sms, stream)
+                  : launch_one<kCopyRow, false>(a, num_sms, stream);
+}
+
+}  // namespace ep

@@ -1,0 +1,109 @@
+// Internal declarations shared by the kernels and the C-ABI layer.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ep_get.h"
+
+namespace ep {
+
+constexpr int kLayoutThreads = 256;  // one thread per token in the layout kernels
+constexpr int kBlockTokens = kLayoutThreads;
+constexpr int kLayoutWarps = kLayoutThreads / 32;
+constexpr int kMaxRanks = 64;
+constexpr int kMaxTopk = 32;
+constexpr int kMaxExperts = 4096;
+constexpr int kMaxScaleGroups = 128;  // FP8 receive: hidden <= 128 * 128
+constexpr int kCopyThreads = 256;     // dispatch / combine CTA size (8 warps)
+constexpr int kMaxPrologueCtas = 64;
+
+// device error bits latched in the workspace header
+constexpr uint32_t kErrBadTopk = 1u;
+constexpr uint32_t kErrOverflow = 2u;
+
+// Sizes derived from an ep_config_t that passed validation.
+struct Geometry {
+  int R, n_so, n_su, E, L, K, T, M, H, G, NB;
+  int x_fp8, recv_fp8, expand, align;
+  int64_t region_rows;  // rows of one destination region in the row form: R * M
+  int64_t num_tokens;   // R * T
+};
+
+// Byte offsets of the workspace pieces.
+struct Workspace {
+  size_t err;         // uint32: sticky device error bits
+  size_t done;        // uint32: arrival counter of the scan kernel (returns to 0)
+  size_t blk_cnt;     // int32 [R][NB][R]   per-block destination counts
+  size_t blk_base;    // int32 [R][NB][R]   per-block first row inside the region
+  size_t blk_cnt_e;   // int32 [R][NB][E]   per-block expert counts
+  size_t blk_base_e;  // int32 [R][NB][E]   per-block first expanded row (expand)
+  size_t total;
+};
+
+Workspace workspace_layout(const Geometry& g);
+int make_geometry(const ep_config_t* cfg, Geometry* g);  // returns EP_OK or an error
+
+struct LayoutArgs {
+  const int64_t* topk_idx;
+  int32_t* num_tokens_per_rank;
+  int32_t* num_tokens_per_expert;
+  uint8_t* is_token_in_rank;
+  int32_t* slot_map;
+  int32_t* recv_cnt;
+  int32_t* recv_psum;
+  int32_t* exp_cnt;
+  int32_t* exp_base;
+  int32_t* exp_region;
+  int32_t* exp_pos;
+  uint32_t* err;
+  uint32_t* done;
+  int32_t* blk_cnt;
+  int32_t* blk_base;
+  int32_t* blk_cnt_e;
+  int32_t* blk_base_e;
+  int R, n_so, n_su, E, L, K, T, M, NB, expand, align;
+};
+
+struct DispatchArgs {
+  const uint8_t* x;
+  const float* x_sf;
+  const int64_t* topk_idx;
+  const float* topk_w;
+  const int32_t* slot_map;
+  const int32_t* exp_pos;
+  const int32_t* exp_region;
+  uint8_t* recv_x;
+  float* recv_sf;
+  int64_t* recv_idx;
+  float* recv_w;
+  int32_t* recv_md;
+  int R, E, L, K, T, H, G;
+  int64_t region_rows;
+  int64_t num_tokens;
+  int in_row_bytes, out_row_bytes;
+};
+
+struct CombineArgs {
+  const uint16_t* y;
+  const int64_t* topk_idx;
+  const float* topk_w;
+  const int32_t* slot_map;
+  const int32_t* exp_pos;
+  const int32_t* exp_region;
+  uint16_t* out;
+  int E, L, K, T, H;
+  int64_t region_rows;
+  int64_t num_tokens;
+};
+
+cudaError_t launch_layout(const Geometry& g, const LayoutArgs& a, int num_prologue_sms,
+                          cudaStream_t stream);
+cudaError_t launch_dispatch(const Geometry& g, const DispatchArgs& a, int num_sms,
+                            cudaStream_t stream);
+cudaError_t launch_combine(const Geometry& g, const CombineArgs& a, int num_sms,
+                           cudaStream_t stream);
+
+int device_sm_count();
+
+}  // namespace ep

@@ -1,0 +1,196 @@
+/*
+ * ep_get.h — C ABI of a single-GPU MoE expert-parallel token dispatch / combine.
+ *
+ * The EP ranks are logical partitions of one GPU's memory: rank r's tokens are
+ * rows [r*T, (r+1)*T) of the inputs, and rank r's receive buffer is region r of
+ * the receive tensors. Every move is a device-memory scatter or gather on the
+ * caller's stream.
+ *
+ * Sources (DeepEP issue and pull-request pages):
+ *   [P753] PR #753 "Kernel-side deterministic dispatch for the non-expand
+ *          layout": Motivation, Approach, "Direct vs hybrid dispatch",
+ *          Compatibility, "New API".
+ *   [P690] PR #690 "Add Direct Recv X dispatch path": review comments on the
+ *          copy epilogue and the buffer sizing; Summary; Implementation.
+ *   [P544] PR #544 "Fix duplicate calculation of num_tokens_per_rank" (title,
+ *          cited from the footer of issue #647).
+ *
+ * Conventions for every entry point:
+ *   - Pointers named "device" must point to device memory of the current CUDA
+ *     device; the caller owns and allocates every buffer, including the
+ *     workspace. The library never allocates, frees or synchronises, except
+ *     ep_check_error, which synchronises the given stream.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream). All work
+ *     is enqueued asynchronously on it, in call order.
+ *   - Returns EP_OK (0) or a negative EP_ERR_* code. Host-detectable errors are
+ *     reported before anything is enqueued. Errors found on the device (bad
+ *     top-k values) are latched in the workspace and read by ep_check_error.
+ *     Unsupported combinations return EP_ERR_UNSUPPORTED; nothing is ever
+ *     dropped silently.
+ *   - All row pointers must be 16-byte aligned.
+ */
+#ifndef EP_GET_H_
+#define EP_GET_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes -------------------------------------------------------- */
+#define EP_OK 0
+#define EP_ERR_INVALID_ARG (-1) /* bad size, null or misaligned pointer      */
+#define EP_ERR_UNSUPPORTED (-2) /* valid request this library does not do    */
+#define EP_ERR_WORKSPACE (-3)   /* workspace missing or smaller than needed  */
+#define EP_ERR_CUDA (-4)        /* a CUDA launch or runtime call failed      */
+#define EP_ERR_BAD_TOPK (-5)    /* device: top-k value < -1 or >= num_experts,
+                                   or a repeated expert in the expanded layout */
+#define EP_ERR_OVERFLOW (-6)    /* a row would not fit (cannot happen when
+                                   num_tokens <= num_max_tokens_per_rank)   */
+
+/* ---- element types ------------------------------------------------------- */
+#define EP_DTYPE_BF16 0
+#define EP_DTYPE_FP8_E4M3 1 /* OCP E4M3 ("FN"), fp32 scale per 128 columns */
+
+/* ---- configuration --------------------------------------------------------
+ * Ranks: R = num_scaleout_ranks * num_scaleup_ranks; global rank
+ * r = scaleout * num_scaleup_ranks + scaleup. num_scaleout_ranks == 1 is the
+ * direct layout, > 1 the hybrid row form [P753 "Direct vs hybrid dispatch"].
+ * Experts: expert e lives on rank e / (num_experts / R).
+ */
+typedef struct ep_config {
+  int32_t num_scaleout_ranks;      /* >= 1; 1 = direct                           */
+  int32_t num_scaleup_ranks;       /* >= 1; R <= 64                              */
+  int32_t num_experts;             /* multiple of R                              */
+  int32_t num_topk;                /* K, 1..32                                   */
+  int32_t num_tokens;              /* T per logical rank, 0..num_max_tokens_per_rank */
+  int32_t num_max_tokens_per_rank; /* M >= 1                                     */
+  int32_t hidden;                  /* H; multiple of 8 (bf16), of 128 with FP8   */
+  int32_t x_dtype;                 /* EP_DTYPE_BF16, or EP_DTYPE_FP8_E4M3 (pre-cast x + x_sf) */
+  int32_t recv_dtype;              /* EP_DTYPE_BF16, or EP_DTYPE_FP8_E4M3 (cast inside dispatch
+                                      when x is bf16)                            */
+  int32_t expand;                  /* 0 = row form, 1 = expanded per-expert blocks */
+  int32_t expert_alignment;        /* >= 1: expanded blocks padded to a multiple */
+  int32_t num_sms;                 /* SMs for dispatch/combine; 0 = all          */
+  int32_t num_prologue_sms;        /* SMs for the layout prologue; 0 = automatic;
+                                      capped at 64 [P753 "New API"]. Results never
+                                      depend on it.                              */
+} ep_config_t;
+
+/* ---- dispatch layout (all device pointers, int32 unless noted) -------------
+ * Row form: destination d's region of the receive tensors has R*M rows; source
+ * s owns the M rows starting at row_block(s)*M, where row_block(s) = s
+ * (direct) or scaleup(s)*num_scaleout_ranks + scaleout(s) (hybrid: segment =
+ * source scale-up rank, in-segment offset = source scale-out rank * M + slot)
+ * [P753 Approach; "Direct vs hybrid dispatch"].
+ */
+typedef struct ep_layout {
+  int32_t* num_tokens_per_rank;   /* [R src][R dst]: tokens of src reaching dst,
+                                     once per token [P544]                      */
+  int32_t* num_tokens_per_expert; /* [R src][E]: valid lanes per expert         */
+  uint8_t* is_token_in_rank;      /* [R][T][R dst]: 0/1                          */
+  int32_t* slot_map;              /* [R][T][K]: row inside the destination region =
+                                     row_block(src)*M + the source's running count of
+                                     deduplicated entries to that destination in token
+                                     order; lanes to the same destination share it;
+                                     -1 for masked lanes [P753 Approach]         */
+  int32_t* recv_cnt;              /* [R dst][R src] = num_tokens_per_rank transposed */
+  int32_t* recv_psum;             /* [R dst][R row blocks]: inclusive prefix sums of
+                                     recv_cnt in row-block order [P753 "Direct vs
+                                     hybrid dispatch": per-source receive counts] */
+  /* expanded layout only (may be NULL when expand == 0): per destination, per
+     local expert j, a block of rows holding that expert's lanes in (source rank,
+     token) order, padded to expert_alignment; regions concatenated by rank. */
+  int32_t* exp_cnt;    /* [R][L]: lanes per (destination, local expert)         */
+  int32_t* exp_base;   /* [R][L+1]: block starts inside the region; [L] = size  */
+  int32_t* exp_region; /* [R+1]: first row of each region; [R] = total rows     */
+  int32_t* exp_pos;    /* [R][T][K]: row of the lane inside its destination's
+                          region, -1 for masked lanes                          */
+} ep_layout_t;
+
+/* ---- receive buffers (device pointers) -------------------------------------
+ * Row form: recv_x/recv_sf rows are indexed d*R*M + slot. Expanded: recv_x and
+ * recv_sf rows are indexed exp_region[d] + exp_pos. The sidecars are always row
+ * form. Rows no entry fills are left untouched. recv_topk_idx,
+ * recv_topk_weights and recv_src_metadata may be NULL (not written).
+ */
+typedef struct ep_recv {
+  void* recv_x;                /* [recv_x_rows][H] bf16 or e4m3                 */
+  float* recv_sf;              /* [recv_x_rows][H/128] (FP8 receive only)       */
+  int64_t* recv_topk_idx;      /* [R][R*M][K]: destination-local expert or -1    */
+  float* recv_topk_weights;    /* [R][R*M][K]: weight, or 0 off this destination */
+  int32_t* recv_src_metadata;  /* [R][R*M][2+K]: {src rank, src token,
+                                  dst_tensor_idx[K]}; field 2+k = expanded row of
+                                  lane k in this destination's region, else -1
+                                  [P690 copy-epilogue review]                   */
+  int64_t recv_x_rows;         /* capacity of recv_x in rows, >= ep_recv_rows()  */
+} ep_recv_t;
+
+/* Workspace bytes the three entry points need for this configuration. The
+ * workspace must be zero-filled before its first use (ep_workspace_init or a
+ * zeroing allocator); afterwards the library keeps it consistent. One
+ * workspace serves one stream at a time. */
+size_t ep_workspace_bytes(const ep_config_t* cfg);
+
+/* Rows the receive buffer recv_x needs: R*R*M (row form; the per-destination
+ * window of [P690]'s buffer sizing times R), or R*T*K + E*(expert_alignment-1)
+ * (expanded upper bound). Returns -1 for an invalid configuration. */
+int64_t ep_recv_rows(const ep_config_t* cfg);
+
+/* Zero the workspace on `stream`. */
+int ep_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/* Dispatch layout [P753 Motivation, Approach]: turns topk_idx (device, int64
+ * [R][T][K]; -1 = masked lane) into the counts, the per-lane slots and, when
+ * expanding, the per-expert positions of `layout` (all device outputs). Three
+ * kernels: a per-block count, a grid-wide scan, then per-lane slots; the
+ * result is a pure function of topk_idx. */
+int ep_get_dispatch_layout(const ep_config_t* cfg, const int64_t* topk_idx,
+                           const ep_layout_t* layout, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/* Dispatch: for every deduplicated (token, destination) entry writes the
+ * token's hidden row into the destination's receive rows at its slot (row
+ * form) or, expanded, one row per valid lane at its position; plus the
+ * sidecars [P753 Approach; P690 Summary/Implementation].
+ *   x: device [R][T][H] bf16 (x_dtype BF16) or e4m3 codes (FP8).
+ *   x_sf: device [R][T][H/128] fp32, FP8 input only (else NULL).
+ *   recv_dtype FP8 with bf16 x casts inside the copy: per 128 columns,
+ *   amax = max(max|x|, 1e-4), sf = amax/448, q = e4m3_rn_satfinite(x*(448/amax)).
+ *   topk_idx / topk_weights: device [R][T][K] int64 / fp32.
+ * `layout` must come from ep_get_dispatch_layout with the same cfg/topk_idx. */
+int ep_dispatch(const ep_config_t* cfg, const ep_layout_t* layout, const void* x,
+                const float* x_sf, const int64_t* topk_idx, const float* topk_weights,
+                const ep_recv_t* recv, void* workspace, size_t workspace_bytes,
+                void* stream);
+
+/* Combine: out[s][t] = bf16_rn(acc), acc = +0 then, for k in lane order over
+ * the valid lanes, acc = fma(topk_weights[s][t][k], y[row of lane k], acc),
+ * in fp32. y: device bf16 expert outputs in the receive layout (row form
+ * [R][R*M][H], or expanded [rows][H]); out: device bf16 [R][T][H]. The result
+ * is bitwise reproducible. */
+int ep_combine(const ep_config_t* cfg, const ep_layout_t* layout, const uint16_t* y,
+               const int64_t* topk_idx, const float* topk_weights, uint16_t* out,
+               void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronises `stream`, returns the first device-detected error latched in
+ * the workspace since the last call (EP_OK if none) and clears it. */
+int ep_check_error(void* workspace, void* stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* ep_status_string(int status);
+
+/* Diagnostics: the device's fp32 -> e4m3 (round to nearest even, saturating)
+ * and fp32 -> bf16 (round to nearest even) conversions used by the kernels,
+ * applied to the binary32 bit patterns first .. first+n-1; out is device
+ * memory of n bytes / n uint16. */
+int ep_diag_e4m3_of_bits(uint32_t first, int64_t n, uint8_t* out, void* stream);
+int ep_diag_bf16_of_bits(uint32_t first, int64_t n, uint16_t* out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EP_GET_H_ */

@@ -60,6 +60,8 @@ def lib():
         L.orc_dispatch.argtypes = [P] * 13
         L.orc_combine_token.restype = None
         L.orc_combine_token.argtypes = [C.c_int, C.c_int, P, P, P]
+        L.orc_combine_gathered.restype = None
+        L.orc_combine_gathered.argtypes = [C.c_int, C.c_int, C.c_int64, P, P, P, P]
         L.orc_combine.restype = C.c_int
         L.orc_combine.argtypes = [P] * 8
         _lib = L
@@ -249,6 +251,34 @@ def combine_token(rows, w):
     out = np.zeros(H, np.uint16)
     lib().orc_combine_token(K, H, ptrs, _p(np.ascontiguousarray(w, dtype=np.float32)), _p(out))
     return out
+
+
+def combine_gathered(lane_rows, y, w):
+    """Combine of n tokens: lane_rows [n, K] int64 rows of y (bf16 bits [rows, H]),
+    -1 for masked lanes; w [n, K] fp32. Returns uint16 [n, H]."""
+    lane_rows = np.ascontiguousarray(lane_rows, dtype=np.int64)
+    n, K = lane_rows.shape
+    ya = _np(y, np.uint16)
+    H = ya.shape[-1]
+    out = np.zeros((n, H), np.uint16)
+    lib().orc_combine_gathered(K, H, n, _p(lane_rows), _p(ya), _p(_np(w, np.float32)), _p(out))
+    return out
+
+
+def global_rows(wl, lay, topk_idx):
+    """Row of every lane in the receive layout: d*R*M + slot (row form) or
+    exp_region[d] + exp_pos (expanded); -1 for masked lanes. int64 [R, T, K]."""
+    idx = _np(topk_idx, np.int64)
+    R = wl.num_ranks
+    L = wl.num_experts // R
+    d = np.where(idx >= 0, idx // L, 0)
+    if wl.expand:
+        r = lay["exp_region"][d].astype(np.int64) + lay["exp_pos"]
+        ok = lay["exp_pos"] >= 0
+    else:
+        r = d * (R * wl.num_max_tokens_per_rank) + lay["slot_map"]
+        ok = lay["slot_map"] >= 0
+    return np.where(ok & (idx >= 0), r, -1).astype(np.int64)
 
 
 def combine(wl, lay, y, topk_idx, topk_weights):

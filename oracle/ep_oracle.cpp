@@ -468,6 +468,20 @@ void orc_combine_token(int K, int H, const uint16_t* const* rows, const float* w
   }
 }
 
+// Combine of n tokens whose lanes' rows were gathered into one compact array:
+// lane_rows [n][K] indexes rows of y (-1 = masked lane), w [n][K], out [n][H].
+void orc_combine_gathered(int K, int H, int64_t n, const int64_t* lane_rows, const uint16_t* y,
+                          const float* w, uint16_t* out) {
+  std::vector<const uint16_t*> rows(K);
+  for (int64_t i = 0; i < n; ++i) {
+    for (int k = 0; k < K; ++k) {
+      const int64_t r = lane_rows[i * K + k];
+      rows[k] = r < 0 ? nullptr : y + r * H;
+    }
+    orc_combine_token(K, H, rows.data(), w + i * K, out + i * H);
+  }
+}
+
 // Full combine: y holds the expert outputs in the receive layout (row form:
 // destination d's rows start at d*R*M; expanded: at exp_region[d]).
 int orc_combine(const orc_cfg* p, const int32_t* slot_map, const int32_t* exp_pos,

@@ -1,0 +1,141 @@
+"""The C-ABI library without a GPU: it loads, exports every entry point that
+include/ep_get.h declares, sizes buffers by closed forms, and rejects bad
+arguments before touching the device."""
+import ctypes as C
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def ep():
+    from combine_ep_get_02_gb300 import _build
+    _build.build()
+    import combine_ep_get_02_gb300 as ep
+    ep.lib()
+    return ep
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "ep_get.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\**\s*(ep_[a-z_0-9]+)\s*\(", text, flags=re.M)))
+
+
+def test_every_declared_symbol_is_exported(ep):
+    names = declared_functions()
+    assert {"ep_get_dispatch_layout", "ep_dispatch", "ep_combine", "ep_workspace_bytes",
+            "ep_recv_rows", "ep_check_error", "ep_status_string"} <= set(names)
+    lib = C.CDLL(ep._build.LIB)
+    for n in names:
+        assert hasattr(lib, n), n
+    nm = subprocess.run(["nm", "-D", "--defined-only", ep._build.LIB], capture_output=True, text=True).stdout
+    exported = set(re.findall(r" T (ep_\w+)$", nm, flags=re.M))
+    assert set(names) <= exported
+
+
+def cfg(ep, **kw):
+    base = dict(num_scaleout_ranks=1, num_scaleup_ranks=16, num_experts=256, num_topk=8,
+                num_tokens=4096, num_max_tokens_per_rank=4096, hidden=7168)
+    base.update(kw)
+    return ep.Config(**base)
+
+
+def test_recv_rows_closed_forms(ep):
+    # row form: R regions of R*M rows (the per-destination window R*M rows)
+    assert ep.ep_recv_rows(cfg(ep)) == 16 * 16 * 4096
+    assert ep.ep_recv_rows(cfg(ep, num_scaleout_ranks=4, num_scaleup_ranks=8, num_tokens=2048,
+                                num_max_tokens_per_rank=2048)) == 32 * 32 * 2048
+    # expanded: every lane plus the worst-case padding of every expert block
+    assert ep.ep_recv_rows(cfg(ep, expand=1)) == 16 * 4096 * 8
+    assert ep.ep_recv_rows(cfg(ep, expand=1, expert_alignment=128)) == 16 * 4096 * 8 + 256 * 127
+
+
+def test_workspace_bytes_closed_form(ep):
+    def expect(R, T, E, expand):
+        NB = -(-T // 256)
+        a = lambda v: (v + 255) // 256 * 256
+        return 256 + 2 * a(4 * R * NB * R) + a(4 * R * NB * E) + (a(4 * R * NB * E) if expand else 0)
+    assert ep.ep_workspace_bytes(cfg(ep)) == expect(16, 4096, 256, False)
+    assert ep.ep_workspace_bytes(cfg(ep, expand=1)) == expect(16, 4096, 256, True)
+    assert ep.ep_workspace_bytes(cfg(ep, num_scaleup_ranks=64, num_experts=512, num_tokens=513,
+                                     num_max_tokens_per_rank=600, expand=1)) == expect(64, 513, 512, True)
+    assert ep.ep_workspace_bytes(cfg(ep, num_tokens=0)) == 256
+
+
+@pytest.mark.parametrize("bad,code", [
+    (dict(num_scaleup_ranks=0), -1),
+    (dict(num_experts=250), -1),              # not a multiple of R
+    (dict(num_tokens=5000), -1),              # T > M
+    (dict(num_topk=0), -1),
+    (dict(num_topk=33), -1),
+    (dict(hidden=100), -1),                   # not a multiple of 8
+    (dict(hidden=1000, recv_dtype=1), -1),    # FP8 needs a multiple of 128
+    (dict(x_dtype=1, recv_dtype=0), -2),      # e4m3 in, bf16 out: not done
+    (dict(num_scaleup_ranks=128, num_experts=256), -2),   # more than 64 ranks
+    (dict(num_experts=8192), -2),
+    (dict(expert_alignment=0), -1),
+    (dict(x_dtype=7), -1),
+])
+def test_invalid_configs_are_rejected_before_any_launch(ep, bad, code):
+    c = cfg(ep, **bad)
+    assert ep.ep_workspace_bytes(c) == 0
+    assert ep.ep_recv_rows(c) == -1
+    cc = c._c()
+    lay = ep._Layout()
+    st = ep.lib().ep_get_dispatch_layout(C.byref(cc), None, C.byref(lay), None, 0, None)
+    assert st == code
+
+
+def test_workspace_checks(ep):
+    c = cfg(ep)
+    cc = c._c()
+    lay = ep._Layout()
+    L = ep.lib()
+    assert L.ep_get_dispatch_layout(C.byref(cc), None, C.byref(lay), None, 1 << 20, None) == ep.EP_ERR_WORKSPACE
+    # misaligned workspace, then one that is too small
+    assert L.ep_get_dispatch_layout(C.byref(cc), None, C.byref(lay), C.c_void_p(0x1008), 1 << 20, None) == ep.EP_ERR_WORKSPACE
+    assert L.ep_get_dispatch_layout(C.byref(cc), None, C.byref(lay), C.c_void_p(0x10000), 16, None) == ep.EP_ERR_WORKSPACE
+    # big enough workspace but missing outputs
+    n = ep.ep_workspace_bytes(c)
+    assert L.ep_get_dispatch_layout(C.byref(cc), C.c_void_p(0x20000), C.byref(lay), C.c_void_p(0x10000), n, None) == ep.EP_ERR_INVALID_ARG
+    assert L.ep_dispatch(C.byref(cc), None, None, None, None, None, None, C.c_void_p(0x10000), n, None) == ep.EP_ERR_INVALID_ARG
+    assert L.ep_combine(C.byref(cc), None, None, None, None, None, C.c_void_p(0x10000), n, None) == ep.EP_ERR_INVALID_ARG
+    assert L.ep_check_error(None, None) == ep.EP_ERR_WORKSPACE
+
+
+def test_misaligned_rows_are_rejected(ep):
+    c = cfg(ep, num_tokens=16, num_max_tokens_per_rank=16, hidden=256)
+    cc = c._c()
+    n = ep.ep_workspace_bytes(c)
+    ws = C.c_void_p(0x100000)
+    lay = ep._Layout(*([C.c_void_p(0x200000)] * 10))
+    recv = ep._Recv(C.c_void_p(0x300008), None, None, None, None, ep.ep_recv_rows(c))  # recv_x not 16-aligned
+    P = C.c_void_p
+    st = ep.lib().ep_dispatch(C.byref(cc), C.byref(lay), P(0x400000), None, P(0x500000), P(0x600000),
+                              C.byref(recv), ws, n, None)
+    assert st == ep.EP_ERR_INVALID_ARG
+    recv = ep._Recv(C.c_void_p(0x300000), None, None, None, None, ep.ep_recv_rows(c) - 1)  # too small
+    st = ep.lib().ep_dispatch(C.byref(cc), C.byref(lay), P(0x400000), None, P(0x500000), P(0x600000),
+                              C.byref(recv), ws, n, None)
+    assert st == ep.EP_ERR_INVALID_ARG
+    st = ep.lib().ep_combine(C.byref(cc), C.byref(lay), P(0x400004), P(0x500000), P(0x600000),
+                             P(0x700000), ws, n, None)
+    assert st == ep.EP_ERR_INVALID_ARG
+
+
+def test_status_strings(ep):
+    assert ep.ep_status_string(0) == "EP_OK"
+    assert ep.ep_status_string(-5) == "EP_ERR_BAD_TOPK"
+    assert ep.ep_status_string(-99) == "EP_ERR_UNKNOWN"
+
+
+def test_product_path_fails_loudly_without_the_library(ep, monkeypatch):
+    monkeypatch.setattr(ep, "_lib", None)
+    monkeypatch.setattr(ep._build, "LIB", "/nonexistent/libep_get.so")
+    with pytest.raises(RuntimeError, match="missing"):
+        ep.lib()

@@ -1,0 +1,239 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle, element
+by element, on seeded inputs of every workload at reduced sizes (several
+256-token blocks, a ragged tail, full hidden widths).
+
+Bar: layouts, slots, receive rows, sidecars and FP8 casts bit-exact; combine
+bit-exact as well (the oracle and the kernel take the same fused multiply-adds
+in the same lane order), which is inside the one-bf16-ulp tolerance.
+"""
+import numpy as np
+import pytest
+import torch
+
+import combine_ep_get_02_gb300 as ep
+import oracle
+import workloads as W
+from _harness import (GpuRun, assert_layout_equal, compare_dispatch, inputs,
+                      oracle_combine_from_device_y, random_y, u16)
+
+pytestmark = pytest.mark.gpu
+
+EXTRA = {
+    # direct with M > T, K=1 and E = R (one expert per rank)
+    "direct_k1_l1": W.Workload("direct_k1_l1", 1, 16, 16, 1, 200, 256, 512),
+    # K above 8 (wide lane path) with masking
+    "direct_k12": W.Workload("direct_k12", 1, 8, 64, 12, 257, 260, 256, mask_frac=0.1),
+    "direct_k32": W.Workload("direct_k32", 1, 4, 64, 32, 70, 70, 128, mask_frac=0.05),
+    # FP8 cast on a width that is not a multiple of 512 columns, heavy masking
+    "cast_h1152": W.Workload("cast_h1152", 1, 8, 64, 6, 513, 520, 1152, recv_dtype="fp8",
+                             mask_frac=0.3, routing="zipf"),
+    # hybrid + expanded + alignment, FP8 cast in the expanded layout
+    "hybrid_expand_a128": W.Workload("hybrid_expand_a128", 2, 4, 64, 4, 300, 300, 256,
+                                     expand=True, expert_alignment=128, routing="zipf",
+                                     y_kind="random"),
+    "expand_fp8": W.Workload("expand_fp8", 1, 8, 32, 4, 260, 260, 512, recv_dtype="fp8",
+                             expand=True, expert_alignment=4, routing="hot", y_kind="random"),
+    # odd sizes: R not a multiple of 4, tiny hidden
+    "odd_r6": W.Workload("odd_r6", 3, 2, 18, 3, 33, 40, 8, mask_frac=0.2),
+    # one token per rank
+    "one_token": W.Workload("one_token", 1, 16, 256, 8, 1, 4, 7168, y_kind="random"),
+}
+
+CASES = dict(W.PARITY)
+CASES.update(EXTRA)
+
+
+@pytest.fixture(scope="module", params=sorted(CASES))
+def case(request):
+    wl = CASES[request.param]
+    idx, w, x, sf = inputs(wl)
+    st, olay = oracle.layout(wl, idx)
+    assert st == 0
+    return wl, idx, w, x, sf, olay
+
+
+def test_layout(case):
+    wl, idx, w, x, sf, olay = case
+    run = GpuRun(wl, idx, w, x, sf).layout()
+    assert run.status() == ep.EP_OK
+    assert_layout_equal(run.layout_np(), olay, wl.expand)
+
+
+def test_dispatch(case):
+    wl, idx, w, x, sf, olay = case
+    run = GpuRun(wl, idx, w, x, sf).layout().dispatch()
+    assert run.status() == ep.EP_OK
+    st, orec = oracle.dispatch(wl, olay, x, sf, idx, w)
+    assert st == 0
+    compare_dispatch(run, olay, orec)
+
+
+def test_combine(case):
+    wl, idx, w, x, sf, olay = case
+    run = GpuRun(wl, idx, w, x, sf).layout()
+    if wl.y_kind == "identity" and wl.recv_dtype == "bf16":
+        run.dispatch()
+        y = run.recv.recv_x
+    else:
+        y = random_y(wl, ep.ep_recv_rows(run.cfg), run.dev)
+    run.combine(y)
+    assert run.status() == ep.EP_OK
+    got = u16(run.out).reshape(-1, wl.hidden)
+    exp = oracle_combine_from_device_y(wl, olay, idx, w, y)
+    if not np.array_equal(got, exp):
+        bad = np.argwhere(got != exp)
+        raise AssertionError(f"{len(bad)} combine mismatches; first {bad[0].tolist()}: "
+                             f"{got[tuple(bad[0])]:#06x} vs {exp[tuple(bad[0])]:#06x}")
+
+
+def test_identity_combine_of_dispatch_is_weight_sum_times_x():
+    """combine(dispatch(x)) with identity experts = (sum of weights) * x, within
+    one bf16 ulp (closed form, independent of the oracle)."""
+    wl = W.PARITY["direct_zipf"]
+    idx, w, x, sf = inputs(wl)
+    run = GpuRun(wl, idx, w, x, sf).layout().dispatch()
+    run.combine(run.recv.recv_x)
+    got = run.out.float().cpu().double()
+    wsum = torch.where(idx >= 0, w.double(), torch.zeros((), dtype=torch.float64)).sum(-1, keepdim=True)
+    closed = wsum * x.double()
+    ulp = torch.where(closed != 0, 2.0 ** (torch.floor(torch.log2(closed.abs().clamp_min(1e-30))) - 7),
+                      torch.full_like(closed, 2.0 ** -133))
+    assert torch.all((got - closed).abs() <= ulp)
+
+
+@pytest.mark.parametrize("name", ["direct_zipf", "hybrid_rowform", "expanded"])
+def test_grid_sizes_do_not_change_results(name):
+    """Slots are a pure function of topk_idx: outputs are identical for every
+    prologue grid and every dispatch/combine grid (PR #753 Approach, New API)."""
+    wl = W.PARITY[name]
+    idx, w, x, sf = inputs(wl)
+    ref = None
+    for pro, sms in ((0, 0), (1, 1), (7, 13), (64, 3), (3, 152)):
+        run = GpuRun(wl, idx, w, x, sf, num_prologue_sms=pro, num_sms=sms).layout().dispatch()
+        y = run.recv.recv_x if not wl.expand else random_y(wl, ep.ep_recv_rows(run.cfg), run.dev)
+        run.combine(y)
+        assert run.status() == ep.EP_OK
+        lay = run.layout_np()
+        rx = u16(run.recv.recv_x)
+        md = run.recv.recv_src_metadata.cpu().numpy()
+        out = u16(run.out)
+        if ref is None:
+            ref = (lay, rx, md, out)
+            continue
+        assert_layout_equal(lay, ref[0], wl.expand)
+        assert np.array_equal(rx, ref[1])
+        assert np.array_equal(md, ref[2])
+        assert np.array_equal(out, ref[3])
+
+
+def test_repeated_runs_bitwise_equal():
+    wl = W.PARITY["dsv3_fp8"]
+    idx, w, x, sf = inputs(wl)
+    run = GpuRun(wl, idx, w, x, sf).layout().dispatch()
+    y = random_y(wl, ep.ep_recv_rows(run.cfg), run.dev)
+    run.combine(y)
+    first = (u16(run.recv.recv_x), run.recv.recv_sf.cpu().numpy(), u16(run.out))
+    for _ in range(3):
+        run.layout().dispatch().combine(y)
+        assert np.array_equal(u16(run.recv.recv_x), first[0])
+        assert np.array_equal(run.recv.recv_sf.cpu().numpy(), first[1])
+        assert np.array_equal(u16(run.out), first[2])
+
+
+def test_slots_do_not_depend_on_x_or_weights():
+    wl = W.PARITY["direct_zipf"]
+    idx, w, x, sf = inputs(wl)
+    a = GpuRun(wl, idx, w, x, sf).layout().layout_np()
+    x2 = torch.randn(x.shape, generator=torch.Generator().manual_seed(5)).to(torch.bfloat16)
+    b = GpuRun(wl, idx, torch.rand_like(w), x2, sf).layout().layout_np()
+    assert_layout_equal(a, b, False)
+
+
+def test_empty_ranks():
+    wl = W.Workload("empty", 1, 8, 32, 4, 0, 16, 256)
+    idx = torch.zeros(8, 0, 4, dtype=torch.int64)
+    w = torch.zeros(8, 0, 4)
+    x = torch.zeros(8, 0, 256, dtype=torch.bfloat16)
+    run = GpuRun(wl, idx, w, x, None).layout().dispatch()
+    run.combine(run.recv.recv_x)
+    assert run.status() == ep.EP_OK
+    lay = run.layout_np()
+    assert not lay["num_tokens_per_rank"].any() and not lay["recv_psum"].any()
+    assert not lay["num_tokens_per_expert"].any()
+
+
+def test_all_lanes_masked():
+    wl = W.Workload("masked", 1, 4, 16, 3, 40, 40, 128)
+    idx = torch.full((4, 40, 3), -1, dtype=torch.int64)
+    w = torch.zeros(4, 40, 3)
+    x = torch.randn(4, 40, 128).to(torch.bfloat16)
+    run = GpuRun(wl, idx, w, x, None).layout().dispatch()
+    run.combine(run.recv.recv_x)
+    assert run.status() == ep.EP_OK
+    assert (run.lay.slot_map == -1).all()
+    assert not u16(run.out).any()  # +0 everywhere
+    assert not u16(run.recv.recv_x).any()  # nothing written (buffer was zeroed)
+
+
+def test_bad_topk_is_reported_not_written():
+    wl = W.Workload("bad", 1, 4, 16, 2, 30, 30, 128)
+    idx, w, x, sf = inputs(wl)
+    idx = idx.clone()
+    idx[1, 3, 0] = 16      # >= E
+    idx[2, 7, 1] = -5      # < -1
+    run = GpuRun(wl, idx, w, x, sf).layout().dispatch()
+    run.combine(run.recv.recv_x)
+    assert run.status() == ep.EP_ERR_BAD_TOPK
+    assert run.status() == ep.EP_OK  # the status is cleared once read
+    # the bad lanes are masked, everything else matches the oracle
+    st, olay = oracle.layout(wl, idx)
+    assert st == oracle.BAD_TOPK
+    assert_layout_equal(run.layout_np(), olay, False)
+
+
+def test_expanded_repeated_expert_is_reported():
+    wl = W.Workload("dup", 1, 4, 16, 3, 20, 20, 128, expand=True)
+    idx, w, x, sf = inputs(wl)
+    idx = idx.clone()
+    idx[0, 2, 2] = idx[0, 2, 0]
+    run = GpuRun(wl, idx, w, x, sf).layout().dispatch()
+    assert run.status() == ep.EP_ERR_BAD_TOPK
+    st, olay = oracle.layout(wl, idx)
+    assert_layout_equal(run.layout_np(), olay, True)
+
+
+def _non_nan_slices(first, n):
+    """Slices of [first, first+n) that hold no NaN bit pattern."""
+    out, lo = [], first
+    for nan_lo, nan_hi in ((0x7F800001, 0x80000000), (0xFF800001, 0x100000000)):
+        if nan_hi <= first or nan_lo >= first + n:
+            continue
+        if nan_lo > lo:
+            out.append(slice(lo - first, nan_lo - first))
+        lo = max(lo, nan_hi)
+    if lo < first + n:
+        out.append(slice(lo - first, n))
+    return out
+
+
+@pytest.mark.parametrize("kind", ["e4m3", "bf16"])
+def test_device_conversions_match_oracle_on_every_float(kind):
+    """The kernels' fp32->e4m3 (RNE, satfinite) and fp32->bf16 (RNE) conversions
+    against the oracle's converters (written from the format definitions) on all
+    2^32 binary32 bit patterns (NaN inputs excluded: outside the contract)."""
+    import concurrent.futures
+    chunk = 1 << 28
+    firsts = list(range(0, 1 << 32, chunk))
+    conv = oracle.e4m3_of_bits if kind == "e4m3" else oracle.bf16_of_bits
+    diag = ep.ep_diag_e4m3_of_bits if kind == "e4m3" else ep.ep_diag_bf16_of_bits
+    dt = torch.uint8 if kind == "e4m3" else torch.int16
+    buf = torch.empty(chunk, dtype=dt, device="cuda")
+    with concurrent.futures.ThreadPoolExecutor(4) as ex:  # the oracle call releases the GIL
+        futs = {f: ex.submit(conv, f, chunk) for f in firsts}
+        for first in firsts:
+            diag(first, buf)
+            got = buf.cpu().numpy()
+            exp = futs.pop(first).result()
+            got = got.view(exp.dtype)
+            for sl in _non_nan_slices(first, chunk):
+                assert np.array_equal(got[sl], exp[sl]), (hex(first), sl)
