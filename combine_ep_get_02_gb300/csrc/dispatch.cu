@@ -158,10 +158,14 @@ __global__ void __launch_bounds__(kCopyThreads) dispatch_kernel(DispatchArgs a) 
       }
     }
 
-    // sidecar rows of each deduplicated destination (row form)
+    // sidecar rows of each deduplicated destination (row form). Metadata field
+    // f = 2 + k carries lane k's expanded row; with K up to 32 there are up to 34
+    // fields, so a lane writes fields lane and lane + 32.
     if (a.recv_idx != nullptr || a.recv_w != nullptr || a.recv_md != nullptr) {
-      const int md_d = __shfl_up_sync(kFullMask, ln.d, 2);    // lane l: lane l-2's d
-      const int md_pos = __shfl_up_sync(kFullMask, ln.pos, 2);
+      const int f0_d = __shfl_sync(kFullMask, ln.d, (lane - 2) & 31);   // lane f-2 for f = lane
+      const int f0_pos = __shfl_sync(kFullMask, ln.pos, (lane - 2) & 31);
+      const int f1_d = __shfl_sync(kFullMask, ln.d, (lane + 30) & 31);  // f = lane + 32
+      const int f1_pos = __shfl_sync(kFullMask, ln.pos, (lane + 30) & 31);
       unsigned m = ln.rmask;
       while (m) {
         const int rl = __ffs(m) - 1;
@@ -174,12 +178,16 @@ __global__ void __launch_bounds__(kCopyThreads) dispatch_kernel(DispatchArgs a) 
           if (a.recv_idx) a.recv_idx[mrow * a.K + lane] = on ? static_cast<int64_t>(ln.e - dj * a.L) : -1;
           if (a.recv_w) a.recv_w[mrow * a.K + lane] = on ? ln.w : 0.f;
         }
-        if (a.recv_md && lane < a.K + 2) {
-          int v;
-          if (lane == 0) v = s;
-          else if (lane == 1) v = t;
-          else v = (kExpand && md_d == dj) ? md_pos : -1;
-          a.recv_md[mrow * (a.K + 2) + lane] = v;
+        if (a.recv_md) {
+          int32_t* md = a.recv_md + mrow * (a.K + 2);
+          if (lane < a.K + 2) {
+            int v;
+            if (lane == 0) v = s;
+            else if (lane == 1) v = t;
+            else v = (kExpand && f0_d == dj) ? f0_pos : -1;
+            md[lane] = v;
+          }
+          if (lane + 32 < a.K + 2) md[lane + 32] = (kExpand && f1_d == dj) ? f1_pos : -1;
         }
       }
     }
