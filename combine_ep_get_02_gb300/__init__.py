@@ -26,7 +26,7 @@ EP_DTYPE_BF16, EP_DTYPE_FP8_E4M3 = 0, 1
 
 __all__ = [
     "Config", "Layout", "Recv", "EpError", "lib", "ep_workspace_bytes", "ep_recv_rows",
-    "ep_workspace_init", "ep_get_dispatch_layout", "ep_dispatch", "ep_combine", "ep_check_error",
+    "ep_workspace_init", "ep_get_dispatch_layout", "ep_get_dispatch_layout_noalloc", "ep_dispatch", "ep_combine", "ep_check_error",
     "ep_status_string", "ep_diag_e4m3_of_bits", "ep_diag_bf16_of_bits", "alloc_layout", "alloc_recv",
     "alloc_workspace", "config_of",
 ]
@@ -111,6 +111,8 @@ def lib():
         L.ep_workspace_init.argtypes = [P, C.c_size_t, P]
         L.ep_get_dispatch_layout.restype = I
         L.ep_get_dispatch_layout.argtypes = [P, P, P, P, C.c_size_t, P]
+        L.ep_get_dispatch_layout_noalloc.restype = I
+        L.ep_get_dispatch_layout_noalloc.argtypes = [P, P, P, P]
         L.ep_dispatch.restype = I
         L.ep_dispatch.argtypes = [P, P, P, P, P, P, P, P, C.c_size_t, P]
         L.ep_combine.restype = I
@@ -235,6 +237,13 @@ def ep_get_dispatch_layout(cfg: Config, topk_idx: torch.Tensor, layout: Layout, 
     c, l = cfg._c(), layout._c()
     _check(lib().ep_get_dispatch_layout(C.byref(c), _ptr(topk_idx), C.byref(l), _ptr(ws),
                                         ws.numel(), _stream(stream)), "ep_get_dispatch_layout")
+
+
+def ep_get_dispatch_layout_noalloc(cfg: Config, topk_idx: torch.Tensor, layout: Layout, stream=None):
+    """The layout without a caller workspace (fixed scratch inside the library)."""
+    c, l = cfg._c(), layout._c()
+    _check(lib().ep_get_dispatch_layout_noalloc(C.byref(c), _ptr(topk_idx), C.byref(l), _stream(stream)),
+           "ep_get_dispatch_layout_noalloc")
 
 
 def ep_dispatch(cfg: Config, layout: Layout, x: torch.Tensor, x_sf, topk_idx: torch.Tensor,

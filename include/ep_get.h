@@ -151,6 +151,28 @@ int ep_get_dispatch_layout(const ep_config_t* cfg, const int64_t* topk_idx,
                            const ep_layout_t* layout, void* workspace,
                            size_t workspace_bytes, void* stream);
 
+/* Size of the fixed scratch array used by ep_get_dispatch_layout_noalloc. */
+#define EP_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/* ep_get_dispatch_layout for callers that cannot allocate device memory (for
+ * example plugins of inference engines that are handed only their input and
+ * output buffers, or latency-critical code where cudaMalloc is not allowed).
+ * No counterpart on the DeepEP pages: it is the same layout with the workspace
+ * replaced by a fixed array of EP_NOALLOC_SCRATCH_BYTES inside the library,
+ * which every GPU that loads the library keeps until the process exits.
+ *   - Outputs, layout and errors for invalid arguments are those of
+ *     ep_get_dispatch_layout; a configuration whose ep_workspace_bytes exceeds
+ *     EP_NOALLOC_SCRATCH_BYTES returns EP_ERR_WORKSPACE.
+ *   - Allocates nothing. The first call on a device (that device current)
+ *     looks up the array's device address; make it before any stream capture.
+ *   - All calls share the array: each call clears its error bits and counter
+ *     on `stream` first; calls that overlap on the GPU race on it.
+ *   - Invalid top-k values are treated as masked lanes, as in
+ *     ep_get_dispatch_layout, but they are not reported: there is no
+ *     workspace for ep_check_error to read. */
+int ep_get_dispatch_layout_noalloc(const ep_config_t* cfg, const int64_t* topk_idx,
+                                   const ep_layout_t* layout, void* stream);
+
 /* Dispatch: for every deduplicated (token, destination) entry writes the
  * token's hidden row into the destination's receive rows at its slot (row
  * form) or, expanded, one row per valid lane at its position; plus the
