@@ -44,6 +44,8 @@ def parse():
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.WORKLOADS))
     p.add_argument("--tokens", type=int, default=0,
                    help="override tokens per rank (small cases for profiling only)")
+    p.add_argument("--compact", action="store_true",
+                   help="compact receive rows (each destination packed from row 0)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline sample")
@@ -54,12 +56,16 @@ def workload(args):
     wl = W.WORKLOADS[args.workload]
     if args.tokens:
         wl = wl.replace(num_tokens=args.tokens, num_max_tokens_per_rank=max(args.tokens, 1))
+    if args.compact:
+        wl = wl.replace(compact=True)
     return wl
 
 
 def describe(wl) -> str:
     lay = "expanded per-expert blocks" if wl.expand else (
         f"hybrid row form {wl.n_so}x{wl.n_su}" if wl.n_so > 1 else "direct row form")
+    if wl.compact:
+        lay += ", compact receive rows"
     cast = {("bf16", "fp8"): "bf16 x cast to fp8-e4m3 inside dispatch (fp32 scale per 128 columns)",
             ("fp8", "fp8"): "pre-cast fp8-e4m3 x + fp32 scales",
             ("bf16", "bf16"): "bf16 rows"}[(wl.x_dtype, wl.recv_dtype)]
@@ -180,13 +186,19 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(world, v):
+def max_over_ranks(world, v, device="cuda"):
+    """Maximum of a per-rank value over all ranks (the slowest rank's time)."""
     if world == 1:
         return v
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    t = torch.tensor([v], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_rate(world, units_per_rank, total_ms, steps):
+    """Units all ranks processed per second, timed by the slowest rank."""
+    return world * units_per_rank / (total_ms * 1e-3 / steps)
 
 
 def native(args):
@@ -263,10 +275,9 @@ def native(args):
         e2e = end_to_end(ep, cfg, wl, idx_h, w_h, x_h, sf_h, lay, recv, y, identity, ws, stream, dev,
                          args, world)
 
-    n_units = world * R * T
     line = {
         "metric": METRIC,
-        "value": n_units / (total_ms * 1e-3 / args.steps),
+        "value": whole_job_rate(world, R * T, total_ms, args.steps),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": args.steps,

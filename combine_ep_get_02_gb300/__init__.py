@@ -42,7 +42,7 @@ class _Config(C.Structure):
     _fields_ = [(n, C.c_int32) for n in (
         "num_scaleout_ranks", "num_scaleup_ranks", "num_experts", "num_topk", "num_tokens",
         "num_max_tokens_per_rank", "hidden", "x_dtype", "recv_dtype", "expand", "expert_alignment",
-        "num_sms", "num_prologue_sms")]
+        "num_sms", "num_prologue_sms", "compact_recv")]
 
 
 class _Layout(C.Structure):
@@ -72,6 +72,7 @@ class Config:
     expert_alignment: int = 1
     num_sms: int = 0
     num_prologue_sms: int = 0
+    compact_recv: int = 0
 
     @property
     def num_ranks(self) -> int:
@@ -87,7 +88,8 @@ def config_of(wl, **over) -> Config:
                wl.num_max_tokens_per_rank, wl.hidden,
                EP_DTYPE_FP8_E4M3 if wl.x_dtype == "fp8" else EP_DTYPE_BF16,
                EP_DTYPE_FP8_E4M3 if wl.recv_dtype == "fp8" else EP_DTYPE_BF16,
-               int(bool(wl.expand)), wl.expert_alignment)
+               int(bool(wl.expand)), wl.expert_alignment,
+               compact_recv=int(bool(getattr(wl, "compact", False))))
     return dataclasses.replace(c, **over)
 
 

@@ -13,8 +13,6 @@ namespace ep {
 
 namespace {
 
-size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
-
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? EP_OK : EP_ERR_CUDA; }
@@ -74,6 +72,8 @@ int make_geometry(const ep_config_t* c, Geometry* g) {
   if (c->expand != 0 && c->expand != 1) return EP_ERR_INVALID_ARG;
   if (c->expert_alignment < 1) return EP_ERR_INVALID_ARG;
   if (c->num_sms < 0 || c->num_prologue_sms < 0) return EP_ERR_INVALID_ARG;
+  if (c->compact_recv != 0 && c->compact_recv != 1) return EP_ERR_INVALID_ARG;
+  if (c->compact_recv && c->expand) return EP_ERR_UNSUPPORTED;  // expanded rows are packed already
   // 32-bit row indices: rows of one region, lanes, and expanded rows must fit
   const int64_t region_rows = R * c->num_max_tokens_per_rank;
   const int64_t lanes = R * c->num_tokens * c->num_topk;
@@ -90,11 +90,11 @@ int make_geometry(const ep_config_t* c, Geometry* g) {
   g->M = c->num_max_tokens_per_rank;
   g->H = c->hidden;
   g->G = c->hidden / 128;
-  g->NB = (c->num_tokens + kBlockTokens - 1) / kBlockTokens;
   g->x_fp8 = c->x_dtype == EP_DTYPE_FP8_E4M3;
   g->recv_fp8 = c->recv_dtype == EP_DTYPE_FP8_E4M3;
   g->expand = c->expand;
   g->align = c->expert_alignment;
+  g->compact = c->compact_recv;
   g->region_rows = region_rows;
   g->num_tokens = R * c->num_tokens;
   return EP_OK;
@@ -102,21 +102,11 @@ int make_geometry(const ep_config_t* c, Geometry* g) {
 
 Workspace workspace_layout(const Geometry& g) {
   Workspace w;
-  size_t off = 0;
   w.err = 0;
   w.done = 4;
-  off = 256;
-  const size_t blk_r = sizeof(int32_t) * static_cast<size_t>(g.R) * g.NB * g.R;
-  const size_t blk_e = sizeof(int32_t) * static_cast<size_t>(g.R) * g.NB * g.E;
-  w.blk_cnt = off;
-  off = align256(off + blk_r);
-  w.blk_base = off;
-  off = align256(off + blk_r);
-  w.blk_cnt_e = off;
-  off = align256(off + blk_e);
-  w.blk_base_e = off;
-  off = align256(off + (g.expand ? blk_e : 0));
-  w.total = off;
+  w.exp_off = 256;
+  const size_t off_bytes = g.expand ? sizeof(int32_t) * static_cast<size_t>(g.R) * g.E : 0;
+  w.total = 256 + ((off_bytes + 255) & ~static_cast<size_t>(255));
   return w;
 }
 
@@ -201,10 +191,8 @@ int ep_get_dispatch_layout(const ep_config_t* cfg, const int64_t* topk_idx,
   a.exp_pos = layout->exp_pos;
   a.err = at<uint32_t>(workspace, w.err);
   a.done = at<uint32_t>(workspace, w.done);
-  a.blk_cnt = at<int32_t>(workspace, w.blk_cnt);
-  a.blk_base = at<int32_t>(workspace, w.blk_base);
-  a.blk_cnt_e = at<int32_t>(workspace, w.blk_cnt_e);
-  a.blk_base_e = at<int32_t>(workspace, w.blk_base_e);
+  a.exp_off = at<int32_t>(workspace, w.exp_off);
+  a.topk_vec = (g.K % 2 == 0) && aligned(topk_idx, 16);
   a.R = g.R;
   a.n_so = g.n_so;
   a.n_su = g.n_su;
@@ -213,7 +201,6 @@ int ep_get_dispatch_layout(const ep_config_t* cfg, const int64_t* topk_idx,
   a.K = g.K;
   a.T = g.T;
   a.M = g.M;
-  a.NB = g.NB;
   a.expand = g.expand;
   a.align = g.align;
   return cuda_status(launch_layout(g, a, cfg->num_prologue_sms, static_cast<cudaStream_t>(stream)));
@@ -235,6 +222,7 @@ int ep_dispatch(const ep_config_t* cfg, const ep_layout_t* layout, const void* x
   if (g.recv_fp8 && recv->recv_sf == nullptr) return EP_ERR_INVALID_ARG;
   if (g.expand && (layout->exp_pos == nullptr || layout->exp_region == nullptr))
     return EP_ERR_INVALID_ARG;
+  if (g.compact && layout->recv_psum == nullptr) return EP_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(recv->recv_x, 16) || !aligned(topk_idx, 8) ||
       !aligned(topk_weights, 4) || !aligned(x_sf, 4) || !aligned(recv->recv_sf, 4) ||
       !aligned(recv->recv_topk_idx, 8) || !aligned(recv->recv_topk_weights, 4) ||
@@ -252,6 +240,7 @@ int ep_dispatch(const ep_config_t* cfg, const ep_layout_t* layout, const void* x
   a.slot_map = layout->slot_map;
   a.exp_pos = layout->exp_pos;
   a.exp_region = layout->exp_region;
+  a.recv_psum = layout->recv_psum;
   a.recv_x = static_cast<uint8_t*>(recv->recv_x);
   a.recv_sf = recv->recv_sf;
   a.recv_idx = recv->recv_topk_idx;
@@ -264,6 +253,8 @@ int ep_dispatch(const ep_config_t* cfg, const ep_layout_t* layout, const void* x
   a.T = g.T;
   a.H = g.H;
   a.G = g.G;
+  a.M = g.M;
+  a.compact = g.compact;
   a.region_rows = g.region_rows;
   a.num_tokens = g.num_tokens;
   a.in_row_bytes = g.H * (g.x_fp8 ? 1 : 2);
@@ -285,6 +276,7 @@ int ep_combine(const ep_config_t* cfg, const ep_layout_t* layout, const uint16_t
   if (g.expand ? (layout->exp_pos == nullptr || layout->exp_region == nullptr)
                : layout->slot_map == nullptr)
     return EP_ERR_INVALID_ARG;
+  if (g.compact && layout->recv_psum == nullptr) return EP_ERR_INVALID_ARG;
   if (!aligned(y, 16) || !aligned(out, 16) || !aligned(topk_idx, 8) || !aligned(topk_weights, 4))
     return EP_ERR_INVALID_ARG;
   const int sms = sms_or_all(cfg->num_sms);
@@ -296,12 +288,16 @@ int ep_combine(const ep_config_t* cfg, const ep_layout_t* layout, const uint16_t
   a.slot_map = layout->slot_map;
   a.exp_pos = layout->exp_pos;
   a.exp_region = layout->exp_region;
+  a.recv_psum = layout->recv_psum;
   a.out = out;
   a.E = g.E;
   a.L = g.L;
   a.K = g.K;
   a.T = g.T;
   a.H = g.H;
+  a.R = g.R;
+  a.M = g.M;
+  a.compact = g.compact;
   a.region_rows = g.region_rows;
   a.num_tokens = g.num_tokens;
   return cuda_status(launch_combine(g, a, sms, static_cast<cudaStream_t>(stream)));

@@ -35,8 +35,10 @@ __global__ void __launch_bounds__(kCopyThreads) combine_kernel(CombineArgs a) {
         const int r = kExpand ? a.exp_pos[i] : a.slot_map[i];
         if (e >= 0 && e < a.E && r >= 0) {
           const int d = static_cast<int>(e) / a.L;
-          const int64_t row = kExpand ? static_cast<int64_t>(a.exp_region[d]) + r
-                                      : static_cast<int64_t>(d) * a.region_rows + r;
+          const int64_t row =
+              kExpand ? static_cast<int64_t>(a.exp_region[d]) + r
+                      : static_cast<int64_t>(d) * a.region_rows +
+                            recv_row_of_slot(r, d, a.R, a.M, a.compact, a.recv_psum);
           p = a.y + row * a.H;
           w = a.topk_w[i];
         }

@@ -22,6 +22,7 @@ enum Kind { kCopyRow = 0, kCastRow = 1 };
 
 struct TokenLanes {
   int e, d, slot, pos;
+  int row;  // receive row of the lane's deduplicated entry inside its destination region
   float w;
   unsigned vmask;  // valid lanes
   unsigned rmask;  // first lane per destination (deduplicated entries)
@@ -49,6 +50,7 @@ __device__ __forceinline__ TokenLanes load_lanes(const DispatchArgs& a, int64_t 
   const unsigned same = __match_any_sync(kFullMask, L.d);
   L.vmask = __ballot_sync(kFullMask, valid);
   L.rmask = __ballot_sync(kFullMask, valid && (same & lanemask_lt()) == 0);
+  L.row = (valid && !expand) ? recv_row_of_slot(L.slot, L.d, a.R, a.M, a.compact, a.recv_psum) : -1;
   return L;
 }
 
@@ -68,7 +70,7 @@ __global__ void __launch_bounds__(kCopyThreads) dispatch_kernel(DispatchArgs a) 
     const unsigned hmask = kExpand ? ln.vmask : ln.rmask;
     if ((hmask >> lane) & 1) {
       const int64_t row = kExpand ? static_cast<int64_t>(a.exp_region[ln.d]) + ln.pos
-                                  : static_cast<int64_t>(ln.d) * a.region_rows + ln.slot;
+                                  : static_cast<int64_t>(ln.d) * a.region_rows + ln.row;
       s_row[warp][__popc(hmask & lt)] = row;
     }
     __syncwarp();
@@ -171,8 +173,8 @@ __global__ void __launch_bounds__(kCopyThreads) dispatch_kernel(DispatchArgs a) 
         const int rl = __ffs(m) - 1;
         m &= m - 1;
         const int dj = __shfl_sync(kFullMask, ln.d, rl);
-        const int slot = __shfl_sync(kFullMask, ln.slot, rl);
-        const int64_t mrow = static_cast<int64_t>(dj) * a.region_rows + slot;
+        const int row = __shfl_sync(kFullMask, kExpand ? ln.slot : ln.row, rl);
+        const int64_t mrow = static_cast<int64_t>(dj) * a.region_rows + row;
         if (lane < a.K) {
           const bool on = ln.d == dj;
           if (a.recv_idx) a.recv_idx[mrow * a.K + lane] = on ? static_cast<int64_t>(ln.e - dj * a.L) : -1;

@@ -9,7 +9,6 @@
 namespace ep {
 
 constexpr int kLayoutThreads = 256;  // one thread per token in the layout kernels
-constexpr int kBlockTokens = kLayoutThreads;
 constexpr int kLayoutWarps = kLayoutThreads / 32;
 constexpr int kMaxRanks = 64;
 constexpr int kMaxTopk = 32;
@@ -24,20 +23,17 @@ constexpr uint32_t kErrOverflow = 2u;
 
 // Sizes derived from an ep_config_t that passed validation.
 struct Geometry {
-  int R, n_so, n_su, E, L, K, T, M, H, G, NB;
-  int x_fp8, recv_fp8, expand, align;
+  int R, n_so, n_su, E, L, K, T, M, H, G;
+  int x_fp8, recv_fp8, expand, align, compact;
   int64_t region_rows;  // rows of one destination region in the row form: R * M
   int64_t num_tokens;   // R * T
 };
 
 // Byte offsets of the workspace pieces.
 struct Workspace {
-  size_t err;         // uint32: sticky device error bits
-  size_t done;        // uint32: arrival counter of the scan kernel (returns to 0)
-  size_t blk_cnt;     // int32 [R][NB][R]   per-block destination counts
-  size_t blk_base;    // int32 [R][NB][R]   per-block first row inside the region
-  size_t blk_cnt_e;   // int32 [R][NB][E]   per-block expert counts
-  size_t blk_base_e;  // int32 [R][NB][E]   per-block first expanded row (expand)
+  size_t err;      // uint32: sticky device error bits
+  size_t done;     // uint32: arrival counter of the layout kernel (returns to 0)
+  size_t exp_off;  // int32 [R][E]: lanes of each expert from lower source ranks (expand)
   size_t total;
 };
 
@@ -58,11 +54,12 @@ struct LayoutArgs {
   int32_t* exp_pos;
   uint32_t* err;
   uint32_t* done;
-  int32_t* blk_cnt;
-  int32_t* blk_base;
-  int32_t* blk_cnt_e;
-  int32_t* blk_base_e;
-  int R, n_so, n_su, E, L, K, T, M, NB, expand, align;
+  int32_t* exp_off;
+  int R, n_so, n_su, E, L, K, T, M, expand, align;
+  int topk_vec;       // topk_idx rows can be read as 16-byte pairs
+  uint32_t l_magic;   // e / L == __umulhi(e, l_magic) for e, L < 2^16
+  int C;   // CTAs (one cluster) per source rank
+  int TB;  // tokens per CTA
 };
 
 struct DispatchArgs {
@@ -73,12 +70,13 @@ struct DispatchArgs {
   const int32_t* slot_map;
   const int32_t* exp_pos;
   const int32_t* exp_region;
+  const int32_t* recv_psum;  // compact receive rows only
   uint8_t* recv_x;
   float* recv_sf;
   int64_t* recv_idx;
   float* recv_w;
   int32_t* recv_md;
-  int R, E, L, K, T, H, G;
+  int R, E, L, K, T, H, G, M, compact;
   int64_t region_rows;
   int64_t num_tokens;
   int in_row_bytes, out_row_bytes;
@@ -91,8 +89,9 @@ struct CombineArgs {
   const int32_t* slot_map;
   const int32_t* exp_pos;
   const int32_t* exp_region;
+  const int32_t* recv_psum;  // compact receive rows only
   uint16_t* out;
-  int E, L, K, T, H;
+  int E, L, K, T, H, R, M, compact;
   int64_t region_rows;
   int64_t num_tokens;
 };
@@ -105,5 +104,16 @@ cudaError_t launch_combine(const Geometry& g, const CombineArgs& a, int num_sms,
                            cudaStream_t stream);
 
 int device_sm_count();
+
+// Receive row inside destination d's region of a row-form slot: the slot, or
+// (compact) the exclusive prefix of d's receive counts before the slot's row
+// block plus the slot's offset in that block.
+__device__ __forceinline__ int recv_row_of_slot(int slot, int d, int R, int M, int compact,
+                                                const int32_t* recv_psum) {
+  if (!compact) return slot;
+  const int rb = slot / M;
+  const int before = rb == 0 ? 0 : __ldg(recv_psum + d * R + rb - 1);
+  return before + slot - rb * M;
+}
 
 }  // namespace ep

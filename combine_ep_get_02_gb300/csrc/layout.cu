@@ -1,323 +1,454 @@
-// Dispatch layout: per-block counts, a grid-wide scan, then per-lane slots.
+// Dispatch layout: per-warp counts, a scan across the CTAs of each source rank,
+// then per-lane slots.
 //
-// The slot of a (token, destination) entry is the destination row block of its
-// source rank times num_max_tokens_per_rank plus the source's running count of
-// deduplicated entries to that destination in token order (PR #753, Approach).
-// A running count is a prefix sum over tokens, so it is computed as one:
-//   1. layout_count_kernel: each CTA takes a block of 256 tokens of one source
-//      and counts, per destination and per expert, how many of its tokens go
-//      there (warp ballots; one thread per token).
-//   2. layout_scan_kernel: one CTA per source turns the block counts into
-//      exclusive per-block bases and totals; the last CTA to arrive does the
-//      cross-source part (receive counts and their prefix sums, per-expert
-//      block starts of the expanded layout).
-//   3. layout_slot_kernel: each CTA re-derives its tokens' destination sets and
-//      adds the in-block rank (ballot prefix within the warp, then warp prefix
-//      within the block) to the block base.
-// Every value is a pure function of topk_idx: the three grids and the number
-// of CTAs only change who computes what, never the result.
+// The slot of a (token, destination) entry is the row block of its source rank
+// times num_max_tokens_per_rank plus the source's running count of
+// deduplicated entries to that destination in token order (PR #753,
+// Approach). A row block belongs to one source only, so the running count is a
+// prefix sum over that source's own tokens: no information crosses sources.
+//
+// layout_kernel: one thread-block cluster per source rank (up to 8 CTAs, each a
+// contiguous range of the source's tokens, one thread per token per round):
+//   pass 1  each warp counts, per destination, the tokens that reach it
+//           (ballot + popc), and each CTA counts its lanes per expert;
+//   scan    after a cluster barrier every CTA adds up the counts of the CTAs
+//           before it through distributed shared memory: its base per
+//           destination (and, expanded, per expert);
+//   pass 2  warp prefix of the ballots plus the running base gives each lane's
+//           slot; the expanded layout ranks a lane among its expert's lanes with
+//           per-warp bitmaps of the tokens (source-local position).
+// The last CTA of the grid to finish (a counter in the workspace, no waiting)
+// turns the receive counts into their prefix sums.
+// Expanded layout only, two more kernels: layout_expert_scan_kernel scans the
+// per-source expert counts down each expert's column (cross-source offsets and
+// per-expert totals); layout_expand_kernel derives the block starts and region
+// offsets and moves every source-local position to its final row.
+// Every value is a pure function of topk_idx; the grid shape only changes who
+// computes what.
+#include <cooperative_groups.h>
+
 #include "ep_device.cuh"
 #include "ep_internal.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace ep {
 
 namespace {
+
+// e / L for 0 <= e, L <= 4096 as a multiply-high by ceil(2^32 / L), exact in
+// that range; magic == 0 stands for L == 1.
+__device__ __forceinline__ int div_l(int e, uint32_t magic) {
+  return magic == 0 ? e : static_cast<int>(__umulhi(static_cast<uint32_t>(e), magic));
+}
+
+__device__ __forceinline__ bool aligned16(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15) == 0;
+}
 
 // Row block of source s inside every destination region (R blocks of M rows).
 __device__ __forceinline__ int row_block(int s, int n_so, int n_su) {
   return n_so == 1 ? s : (s % n_su) * n_so + s / n_su;
 }
 
-// The CTA's tokens' top-k values, staged transposed ([k][token]) as int32:
-// -1 masked, -2 out of range (an error), else the expert.
-__device__ __forceinline__ void stage_topk(const LayoutArgs& a, int s, int b, int32_t* se) {
-  const int t0 = b * kBlockTokens;
-  const int nt = min(kBlockTokens, a.T - t0);
-  const int64_t base = (static_cast<int64_t>(s) * a.T + t0) * a.K;
-  const int n = nt * a.K;
-  for (int i = threadIdx.x; i < n; i += kLayoutThreads) {
-    const int64_t e = a.topk_idx[base + i];
-    const int t = i / a.K, k = i - t * a.K;
-    se[k * kBlockTokens + t] = (e >= -1 && e < a.E) ? static_cast<int32_t>(e) : -2;
+// One token's top-k lanes in registers: expert per lane, -1 when masked or
+// invalid. Values outside [-1, E) are errors; in the expanded layout so is a
+// repeat of an earlier lane's expert. Returns the destination-rank mask.
+template <int KMAX>
+__device__ __forceinline__ uint64_t load_token(const LayoutArgs& a, int64_t tok, bool live, int (&e)[KMAX],
+                                               bool* bad) {
+  const int64_t* p = a.topk_idx + tok * a.K;
+  int64_t v[KMAX];
+  if (live && a.topk_vec) {
+#pragma unroll
+    for (int k = 0; k < KMAX; k += 2) {
+      if (k < a.K) {
+        const longlong2 q = __ldg(reinterpret_cast<const longlong2*>(p + k));
+        v[k] = q.x;
+        v[k + 1] = q.y;
+      }
+    }
+  } else if (live) {
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k)
+      if (k < a.K) v[k] = __ldg(p + k);
   }
-}
-
-// Destination of lane k of this thread's token, or -1 (masked or invalid).
-// In the expanded layout a repeat of an earlier lane's expert is invalid.
-__device__ __forceinline__ int lane_dst(const LayoutArgs& a, const int32_t* se, int k, int tid,
-                                        bool* bad) {
-  const int e = se[k * kBlockTokens + tid];
-  if (e < 0) {
-    if (e == -2) *bad = true;
-    return -1;
+  uint64_t dmask = 0;
+#pragma unroll
+  for (int k = 0; k < KMAX; ++k) {
+    e[k] = -1;
+    if (live && k < a.K) {
+      const int64_t x = v[k];
+      if (x >= 0 && x < a.E) e[k] = static_cast<int>(x);
+      else if (x != -1) *bad = true;
+    }
   }
   if (a.expand) {
-    for (int j = 0; j < k; ++j) {
-      if (se[j * kBlockTokens + tid] == e) {
-        *bad = true;
-        return -1;
+#pragma unroll
+    for (int k = 1; k < KMAX; ++k) {
+#pragma unroll
+      for (int j = 0; j < k; ++j) {
+        if (e[k] >= 0 && e[j] == e[k]) {
+          e[k] = -1;
+          *bad = true;
+        }
       }
     }
   }
-  return e / a.L;
+#pragma unroll
+  for (int k = 0; k < KMAX; ++k)
+    if (e[k] >= 0) dmask |= 1ull << div_l(e[k], a.l_magic);
+  return dmask;
 }
 
 }  // namespace
 
-// ---- pass 1: per-block counts ----------------------------------------------
-__global__ void __launch_bounds__(kLayoutThreads) layout_count_kernel(LayoutArgs a) {
+// dynamic shared memory: cnt_e [E] | run_e [E] (expand) | ebits [WARPS][E] (expand)
+template <int KMAX, int THREADS>
+__global__ void __launch_bounds__(THREADS) layout_kernel(LayoutArgs a) {
+  constexpr int WARPS = THREADS / 32;
+  cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ int32_t smem[];
-  int32_t* se = smem;                              // [K][256]
-  int32_t* hist = se + a.K * kBlockTokens;         // [E]
-  __shared__ int32_t warp_cnt[kLayoutWarps][kMaxRanks];
+  int32_t* cnt_e = smem;
+  int32_t* run_e = cnt_e + a.E;
+  uint32_t* ebits = reinterpret_cast<uint32_t*>(run_e + a.E);
+  __shared__ int32_t cnt_d[kMaxRanks];
+  __shared__ int32_t run_d[kMaxRanks];
+  __shared__ uint32_t bal[WARPS][kMaxRanks];
+  __shared__ int32_t wbase[WARPS][kMaxRanks];
+  __shared__ int32_t s_cnt[kMaxRanks * kMaxRanks];
+  __shared__ bool s_last;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  for (int e = tid; e < a.E; e += kLayoutThreads) hist[e] = 0;
+  const unsigned lt = lanemask_lt();
+  const int R = a.R, E = a.E;
+  const int s = blockIdx.x / a.C;
+  const int c = static_cast<int>(cluster.block_rank());
+  const int t_begin = min(a.T, c * a.TB), t_end = min(a.T, t_begin + a.TB);
+  const int64_t tok_base = static_cast<int64_t>(s) * a.T;
 
-  const int units = a.R * a.NB;
+  for (int e = tid; e < E; e += THREADS) cnt_e[e] = 0;
+  if (a.expand)
+    for (int i = tid; i < WARPS * E; i += THREADS) ebits[i] = 0;
+  if (tid < R) cnt_d[tid] = 0;
+  __syncthreads();
+
+  // ---- pass 1: this CTA's counts per destination and per expert
   bool bad = false;
-  for (int u = blockIdx.x; u < units; u += gridDim.x) {
-    const int s = u / a.NB, b = u - s * a.NB;
-    __syncthreads();  // previous unit done with se / hist / warp_cnt
-    stage_topk(a, s, b, se);
-    __syncthreads();
-    const bool live = b * kBlockTokens + tid < a.T;
-    uint64_t dmask = 0;
-    if (live) {
-      for (int k = 0; k < a.K; ++k) {
-        const int d = lane_dst(a, se, k, tid, &bad);
-        if (d >= 0) {
-          dmask |= 1ull << d;
-          atomicAdd(&hist[se[k * kBlockTokens + tid]], 1);
-        }
+  {
+    int e[KMAX];
+    int t = t_begin + tid;
+    uint64_t dmask = load_token<KMAX>(a, tok_base + t, t < t_end, e, &bad);
+    for (int t0 = t_begin; t0 < t_end; t0 += THREADS) {
+      // the next round's lanes are in flight while this round is counted
+      int en[KMAX];
+      const int tn = t + THREADS;
+      const uint64_t dn = load_token<KMAX>(a, tok_base + tn, tn < t_end, en, &bad);
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k)
+        if (e[k] >= 0) atomicAdd(&cnt_e[e[k]], 1);
+      const uint32_t lo = static_cast<uint32_t>(dmask), hi = static_cast<uint32_t>(dmask >> 32);
+      for (int d = 0; d < R; ++d) {
+        const int n = __popc(__ballot_sync(kFullMask, ((d < 32 ? lo : hi) >> (d & 31)) & 1u));
+        if (lane == 0 && n != 0) atomicAdd(&cnt_d[d], n);
       }
-    }
-    for (int d = 0; d < a.R; ++d) {
-      const unsigned bal = __ballot_sync(kFullMask, (dmask >> d) & 1);
-      if (lane == 0) warp_cnt[warp][d] = __popc(bal);
-    }
-    __syncthreads();
-    const int64_t blk = static_cast<int64_t>(s) * a.NB + b;
-    for (int d = tid; d < a.R; d += kLayoutThreads) {
-      int c = 0;
-      for (int w = 0; w < kLayoutWarps; ++w) c += warp_cnt[w][d];
-      a.blk_cnt[blk * a.R + d] = c;
-    }
-    for (int e = tid; e < a.E; e += kLayoutThreads) {
-      a.blk_cnt_e[blk * a.E + e] = hist[e];
-      hist[e] = 0;
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k) e[k] = en[k];
+      dmask = dn;
+      t = tn;
     }
   }
   if (bad) atomicOr(a.err, kErrBadTopk);
-}
+  cluster.sync();
 
-// ---- grid-wide scan ---------------------------------------------------------
-// grid = R CTAs (one per source); the last CTA to finish does the cross-source part.
-__global__ void __launch_bounds__(kLayoutThreads) layout_scan_kernel(LayoutArgs a) {
-  extern __shared__ int32_t smem[];
-  __shared__ bool s_last;
-  const int tid = threadIdx.x;
-  const int s = blockIdx.x;
-  const int R = a.R, NB = a.NB, E = a.E;
-
-  // per destination: exclusive per-block bases (absolute rows in the region) and totals
+  // ---- scan across the cluster: counts of the CTAs before this one
   const int rb = row_block(s, a.n_so, a.n_su);
-  for (int d = tid; d < R; d += kLayoutThreads) {
-    int acc = 0;
-    for (int b = 0; b < NB; ++b) {
-      const int64_t i = (static_cast<int64_t>(s) * NB + b) * R + d;
-      const int c = a.blk_cnt[i];
-      a.blk_base[i] = rb * a.M + acc;
-      acc += c;
+  for (int d = tid; d < R; d += THREADS) {
+    int base = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (q < c) base += cluster.map_shared_rank(cnt_d, q)[d];
+    run_d[d] = rb * a.M + base;
+    if (c == a.C - 1) {  // the source's totals
+      const int total = base + cnt_d[d];
+      a.num_tokens_per_rank[s * R + d] = total;
+      a.recv_cnt[d * R + s] = total;
     }
-    a.num_tokens_per_rank[s * R + d] = acc;
-    a.recv_cnt[d * R + s] = acc;
   }
-  // per expert: totals, and (expanded) exclusive per-block prefixes within the source
-  for (int e = tid; e < E; e += kLayoutThreads) {
-    int acc = 0;
-    for (int b = 0; b < NB; ++b) {
-      const int64_t i = (static_cast<int64_t>(s) * NB + b) * E + e;
-      const int c = a.blk_cnt_e[i];
-      if (a.expand) a.blk_base_e[i] = acc;
-      acc += c;
+  for (int e = tid; e < E; e += THREADS) {
+    int base = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (q < c) base += cluster.map_shared_rank(cnt_e, q)[e];
+    if (a.expand) run_e[e] = base;
+    if (c == a.C - 1) a.num_tokens_per_expert[s * E + e] = base + cnt_e[e];
+  }
+  // other CTAs may still read this CTA's counts: they are left untouched, and
+  // the CTA waits for the whole cluster before it exits
+  cluster.barrier_arrive();
+  __syncthreads();
+
+  // ---- pass 2: slots (and source-local expanded positions)
+  {
+    int e[KMAX];
+    bool unused = false;
+    int t = t_begin + tid;
+    uint64_t dmask = load_token<KMAX>(a, tok_base + t, t < t_end, e, &unused);
+    for (int t0 = t_begin; t0 < t_end; t0 += THREADS) {
+      const bool live = t < t_end;
+      int en[KMAX];
+      const int tn = t + THREADS;
+      const uint64_t dn = load_token<KMAX>(a, tok_base + tn, tn < t_end, en, &unused);
+      if (a.expand) {
+#pragma unroll
+        for (int k = 0; k < KMAX; ++k)
+          if (e[k] >= 0) atomicOr(&ebits[warp * E + e[k]], 1u << lane);
+      }
+      const uint32_t lo = static_cast<uint32_t>(dmask), hi = static_cast<uint32_t>(dmask >> 32);
+      for (int d = 0; d < R; ++d) {
+        const uint32_t b = __ballot_sync(kFullMask, ((d < 32 ? lo : hi) >> (d & 31)) & 1u);
+        if (lane == 0) bal[warp][d] = b;
+      }
+      __syncthreads();
+      for (int d = tid; d < R; d += THREADS) {
+        int r = run_d[d];
+#pragma unroll
+        for (int w = 0; w < WARPS; ++w) {
+          wbase[w][d] = r;
+          r += __popc(bal[w][d]);
+        }
+        run_d[d] = r;
+      }
+      __syncthreads();
+      if (live) {
+        const int64_t tok = tok_base + t;
+        int slot[KMAX], pos[KMAX];
+#pragma unroll
+        for (int k = 0; k < KMAX; ++k) {
+          slot[k] = -1;
+          pos[k] = -1;
+          if (e[k] >= 0) {
+            const int d = div_l(e[k], a.l_magic);
+            slot[k] = wbase[warp][d] + __popc(bal[warp][d] & lt);
+            if (a.expand) {
+              int p = run_e[e[k]] + __popc(ebits[warp * E + e[k]] & lt);
+              for (int w = 0; w < warp; ++w) p += __popc(ebits[w * E + e[k]]);
+              pos[k] = p;
+            }
+          }
+        }
+        int32_t* srow = a.slot_map + tok * a.K;
+        int32_t* prow = a.expand ? a.exp_pos + tok * a.K : nullptr;
+        if (a.K == KMAX && (KMAX & 3) == 0 && aligned16(srow) && (prow == nullptr || aligned16(prow))) {
+#pragma unroll
+          for (int k = 0; k < KMAX; k += 4) {
+            *reinterpret_cast<int4*>(srow + k) = make_int4(slot[k], slot[k + 1], slot[k + 2], slot[k + 3]);
+            if (prow) *reinterpret_cast<int4*>(prow + k) = make_int4(pos[k], pos[k + 1], pos[k + 2], pos[k + 3]);
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < KMAX; ++k) {
+            if (k < a.K) {
+              srow[k] = slot[k];
+              if (prow) prow[k] = pos[k];
+            }
+          }
+        }
+        uint8_t* row = a.is_token_in_rank + tok * R;
+        if ((R & 3) == 0) {
+          for (int d = 0; d < R; d += 4) {
+            const uint32_t v = static_cast<uint32_t>((dmask >> d) & 1) |
+                               static_cast<uint32_t>((dmask >> (d + 1)) & 1) << 8 |
+                               static_cast<uint32_t>((dmask >> (d + 2)) & 1) << 16 |
+                               static_cast<uint32_t>((dmask >> (d + 3)) & 1) << 24;
+            *reinterpret_cast<uint32_t*>(row + d) = v;
+          }
+        } else {
+          for (int d = 0; d < R; ++d) row[d] = static_cast<uint8_t>((dmask >> d) & 1);
+        }
+      }
+      if (a.expand) {
+        __syncthreads();
+        for (int x = tid; x < E; x += THREADS) {
+          int n = 0;
+          for (int w = 0; w < WARPS; ++w) {
+            n += __popc(ebits[w * E + x]);
+            ebits[w * E + x] = 0;
+          }
+          run_e[x] += n;
+        }
+      }
+      __syncthreads();
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k) e[k] = en[k];
+      dmask = dn;
+      t = tn;
     }
-    a.num_tokens_per_expert[s * E + e] = acc;
   }
 
+  // ---- the last CTA of the grid: prefix sums of the receive counts
   __threadfence();
-  __syncthreads();
-  if (tid == 0) s_last = atomicAdd(a.done, 1u) == static_cast<unsigned>(gridDim.x) - 1u;
+  cluster.barrier_wait();
+  if (tid == 0) s_last = atomicAdd(a.done, 1u) == gridDim.x - 1u;
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-
-  // receive counts: inclusive prefix over row blocks (block i holds source src(i))
-  for (int d = tid; d < R; d += kLayoutThreads) {
+  for (int i = tid; i < R * R; i += THREADS) s_cnt[i] = ld_cg(a.recv_cnt + i);
+  __syncthreads();
+  for (int d = tid; d < R; d += THREADS) {
     int acc = 0;
-    for (int i = 0; i < R; ++i) {
+    for (int i = 0; i < R; ++i) {  // row block i holds source src(i)
       const int src = a.n_so == 1 ? i : (i % a.n_so) * a.n_su + i / a.n_so;
-      acc += ld_cg(a.recv_cnt + d * R + src);
+      acc += s_cnt[d * R + src];
       a.recv_psum[d * R + i] = acc;
-    }
-  }
-
-  if (a.expand) {
-    int32_t* s_blk = smem;         // [E]: block start of expert e inside its region
-    int32_t* s_size = smem + E;    // [R]: region sizes
-    const int L = a.L;
-    for (int e = tid; e < E; e += kLayoutThreads) {
-      int n = 0;
-      for (int src = 0; src < R; ++src) n += ld_cg(a.num_tokens_per_expert + src * E + e);
-      a.exp_cnt[e] = n;
-      s_blk[e] = n;
-    }
-    __syncthreads();
-    for (int d = tid; d < R; d += kLayoutThreads) {
-      int base = 0;
-      for (int j = 0; j < L; ++j) {
-        const int n = s_blk[d * L + j];
-        a.exp_base[d * (L + 1) + j] = base;
-        s_blk[d * L + j] = base;
-        base += (n + a.align - 1) / a.align * a.align;
-      }
-      a.exp_base[d * (L + 1) + L] = base;
-      s_size[d] = base;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      int acc = 0;
-      for (int d = 0; d < R; ++d) {
-        a.exp_region[d] = acc;
-        acc += s_size[d];
-      }
-      a.exp_region[R] = acc;
-    }
-    // per (source, expert, block): block start + earlier sources' lanes + earlier blocks'
-    for (int e = tid; e < E; e += kLayoutThreads) {
-      int off = s_blk[e];
-      for (int src = 0; src < R; ++src) {
-        for (int b = 0; b < NB; ++b) {
-          const int64_t i = (static_cast<int64_t>(src) * NB + b) * E + e;
-          a.blk_base_e[i] = ld_cg(a.blk_base_e + i) + off;
-        }
-        off += ld_cg(a.num_tokens_per_expert + src * E + e);
-      }
     }
   }
   if (tid == 0) *a.done = 0u;  // ready for the next call
 }
 
-// ---- pass 2: per-lane slots ---------------------------------------------------
-__global__ void __launch_bounds__(kLayoutThreads) layout_slot_kernel(LayoutArgs a) {
+// Expanded layout, step 2: for 32 experts per CTA, the exclusive prefix of the
+// per-source counts down each expert's column (lanes of that expert from lower
+// source ranks) and the column totals.
+__global__ void __launch_bounds__(kLayoutThreads) layout_expert_scan_kernel(LayoutArgs a) {
+  constexpr int kCols = 32, kGroups = kLayoutThreads / kCols;
+  __shared__ int32_t part[kGroups][kCols];
+  const int ci = threadIdx.x % kCols, g = threadIdx.x / kCols;
+  const int e = blockIdx.x * kCols + ci;
+  const int R = a.R, E = a.E;
+  const int per = (R + kGroups - 1) / kGroups;
+  const int s0 = min(R, g * per), s1 = min(R, s0 + per);
+  int v[(kMaxRanks + kGroups - 1) / kGroups];
+  int sum = 0;
+#pragma unroll
+  for (int i = 0; i < (kMaxRanks + kGroups - 1) / kGroups; ++i) {
+    v[i] = (s0 + i < s1 && e < E) ? __ldg(a.num_tokens_per_expert + (s0 + i) * E + e) : 0;
+    sum += v[i];
+  }
+  part[g][ci] = sum;
+  __syncthreads();
+  int acc = 0;
+  for (int q = 0; q < g; ++q) acc += part[q][ci];
+  if (e < E) {
+#pragma unroll
+    for (int i = 0; i < (kMaxRanks + kGroups - 1) / kGroups; ++i) {
+      if (s0 + i < s1) a.exp_off[(s0 + i) * E + e] = acc;
+      acc += v[i];
+    }
+    if (g == kGroups - 1) a.exp_cnt[e] = acc;
+  }
+}
+
+// Expanded layout, step 3: block starts (aligned) and region offsets, then
+// each lane's final row = block start + lower sources' lanes + source-local rank.
+__global__ void __launch_bounds__(kLayoutThreads) layout_expand_kernel(LayoutArgs a) {
   extern __shared__ int32_t smem[];
-  int32_t* se = smem;                                                 // [K][256]
-  uint32_t* ebits = reinterpret_cast<uint32_t*>(se + a.K * kBlockTokens);  // [8][E] (expand)
-  __shared__ uint32_t bal_d[kLayoutWarps][kMaxRanks];
-  __shared__ int32_t base_d[kLayoutWarps][kMaxRanks];
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const unsigned lt = lanemask_lt();
-  if (a.expand)
-    for (int i = tid; i < kLayoutWarps * a.E; i += kLayoutThreads) ebits[i] = 0;
-
-  const int units = a.R * a.NB;
-  for (int u = blockIdx.x; u < units; u += gridDim.x) {
-    const int s = u / a.NB, b = u - s * a.NB;
-    __syncthreads();
-    stage_topk(a, s, b, se);
-    __syncthreads();
-    const int t = b * kBlockTokens + tid;
-    const bool live = t < a.T;
-    bool bad = false;
-    uint64_t dmask = 0;
-    if (live) {
-      for (int k = 0; k < a.K; ++k) {
-        const int d = lane_dst(a, se, k, tid, &bad);
-        if (d >= 0) {
-          dmask |= 1ull << d;
-          if (a.expand) atomicOr(&ebits[warp * a.E + se[k * kBlockTokens + tid]], 1u << lane);
-        }
-      }
+  int32_t* blk = smem;              // [E]: block start of each expert inside its region
+  int32_t* off = smem + a.E;        // [E]: this source's cross-source offsets
+  __shared__ int32_t size_d[kMaxRanks];
+  const int tid = threadIdx.x;
+  const int s = blockIdx.x / a.C, c = blockIdx.x % a.C;
+  const int E = a.E, L = a.L, R = a.R;
+  for (int e = tid; e < E; e += kLayoutThreads) {
+    blk[e] = __ldg(a.exp_cnt + e);
+    off[e] = __ldg(a.exp_off + s * E + e);
+  }
+  __syncthreads();
+  for (int d = tid; d < R; d += kLayoutThreads) {
+    int base = 0;
+    for (int j = 0; j < L; ++j) {
+      const int n = blk[d * L + j];
+      blk[d * L + j] = base;
+      base += (n + a.align - 1) / a.align * a.align;
     }
-    for (int d = 0; d < a.R; ++d) {
-      const unsigned bal = __ballot_sync(kFullMask, (dmask >> d) & 1);
-      if (lane == 0) bal_d[warp][d] = bal;
-    }
-    __syncthreads();
-    const int64_t blk = static_cast<int64_t>(s) * a.NB + b;
-    for (int d = tid; d < a.R; d += kLayoutThreads) {
-      int base = a.blk_base[blk * a.R + d];
-      for (int w = 0; w < kLayoutWarps; ++w) {
-        base_d[w][d] = base;
-        base += __popc(bal_d[w][d]);
+    size_d[d] = base;
+  }
+  __syncthreads();
+  if (blockIdx.x == 0) {  // the tables themselves
+    for (int e = tid; e < E; e += kLayoutThreads) a.exp_base[(e / L) * (L + 1) + e % L] = blk[e];
+    for (int d = tid; d < R; d += kLayoutThreads) a.exp_base[d * (L + 1) + L] = size_d[d];
+    if (tid == 0) {
+      int acc = 0;
+      for (int d = 0; d < R; ++d) {
+        a.exp_region[d] = acc;
+        acc += size_d[d];
       }
+      a.exp_region[R] = acc;
     }
-    __syncthreads();
-    if (live) {
-      const int64_t tok = static_cast<int64_t>(s) * a.T + t;
-      for (int k = 0; k < a.K; ++k) {
-        const int d = lane_dst(a, se, k, tid, &bad);
-        int slot = -1, pos = -1;
-        if (d >= 0) {
-          slot = base_d[warp][d] + __popc(bal_d[warp][d] & lt);
-          if (a.expand) {
-            const int e = se[k * kBlockTokens + tid];
-            pos = a.blk_base_e[blk * a.E + e] + __popc(ebits[warp * a.E + e] & lt);
-            for (int w = 0; w < warp; ++w) pos += __popc(ebits[w * a.E + e]);
-          }
-        }
-        a.slot_map[tok * a.K + k] = slot;
-        if (a.expand) a.exp_pos[tok * a.K + k] = pos;
-      }
-      uint8_t* row = a.is_token_in_rank + tok * a.R;
-      if ((a.R & 3) == 0) {
-        for (int d = 0; d < a.R; d += 4) {
-          const uint32_t v = static_cast<uint32_t>((dmask >> d) & 1) |
-                             static_cast<uint32_t>((dmask >> (d + 1)) & 1) << 8 |
-                             static_cast<uint32_t>((dmask >> (d + 2)) & 1) << 16 |
-                             static_cast<uint32_t>((dmask >> (d + 3)) & 1) << 24;
-          *reinterpret_cast<uint32_t*>(row + d) = v;
-        }
-      } else {
-        for (int d = 0; d < a.R; ++d) row[d] = static_cast<uint8_t>((dmask >> d) & 1);
-      }
-    }
-    if (a.expand) {
-      __syncthreads();
-      for (int i = tid; i < kLayoutWarps * a.E; i += kLayoutThreads) ebits[i] = 0;
+  }
+  const int t_begin = min(a.T, c * a.TB), t_end = min(a.T, t_begin + a.TB);
+  const int64_t i0 = (static_cast<int64_t>(s) * a.T + t_begin) * a.K;
+  const int64_t i1 = (static_cast<int64_t>(s) * a.T + t_end) * a.K;
+  for (int64_t i = i0 + tid; i < i1; i += kLayoutThreads) {
+    const int p = a.exp_pos[i];
+    if (p >= 0) {
+      const int e = static_cast<int>(__ldg(a.topk_idx + i));
+      a.exp_pos[i] = p + blk[e] + off[e];
     }
   }
 }
 
-cudaError_t launch_layout(const Geometry& g, const LayoutArgs& a, int num_prologue_sms,
-                          cudaStream_t stream) {
-  const int units = g.R * g.NB;
-  int ctas = num_prologue_sms > 0 ? num_prologue_sms : kMaxPrologueCtas;
-  ctas = ctas > kMaxPrologueCtas ? kMaxPrologueCtas : ctas;
-  ctas = units < ctas ? units : ctas;
-  const size_t se_bytes = sizeof(int32_t) * g.K * kBlockTokens;
-  const size_t count_smem = se_bytes + sizeof(int32_t) * g.E;
-  const size_t slot_smem = se_bytes + (g.expand ? sizeof(uint32_t) * kLayoutWarps * g.E : 0);
-  const size_t scan_smem = g.expand ? sizeof(int32_t) * (g.E + g.R) : 0;
+namespace {
+
+template <int KMAX, int THREADS>
+cudaError_t launch_main(const Geometry& g, const LayoutArgs& a, cudaStream_t stream) {
+  const size_t smem = sizeof(int32_t) * g.E +
+                      (g.expand ? sizeof(int32_t) * (g.E + static_cast<size_t>(THREADS / 32) * g.E) : 0);
   cudaError_t err;
-  // only requests above the default 48 KB need the opt-in attribute
-  if (count_smem > 48 * 1024 &&
-      (err = cudaFuncSetAttribute(layout_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  static_cast<int>(count_smem))) != cudaSuccess)
+  if (smem > 32 * 1024 &&
+      (err = cudaFuncSetAttribute(layout_kernel<KMAX, THREADS>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(smem))) != cudaSuccess)
     return err;
-  if (slot_smem > 48 * 1024 &&
-      (err = cudaFuncSetAttribute(layout_slot_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  static_cast<int>(slot_smem))) != cudaSuccess)
-    return err;
-  if (ctas > 0) {
-    layout_count_kernel<<<ctas, kLayoutThreads, count_smem, stream>>>(a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(g.R * a.C));
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(a.C);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, layout_kernel<KMAX, THREADS>, a);
+}
+
+}  // namespace
+
+cudaError_t launch_layout(const Geometry& g, const LayoutArgs& args, int num_prologue_sms,
+                          cudaStream_t stream) {
+  LayoutArgs a = args;
+  // one thread per token: 512-thread CTAs (256 when expanding, whose per-warp
+  // expert bitmaps take shared memory), as many CTAs per source as one round
+  // each needs, at most 8 (a portable cluster), within the prologue budget of
+  // 2 CTAs per requested SM and at least one CTA per source
+  const int threads = g.expand ? 256 : 512;
+  const int sms = num_prologue_sms > 0 ? (num_prologue_sms < kMaxPrologueCtas ? num_prologue_sms
+                                                                               : kMaxPrologueCtas)
+                                       : kMaxPrologueCtas;
+  int C = (g.T + threads - 1) / threads;
+  C = C < 1 ? 1 : (C > 8 ? 8 : C);
+  const int budget = (2 * sms) / g.R;
+  if (C > budget) C = budget < 1 ? 1 : budget;
+  a.C = C;
+  a.TB = (g.T + C - 1) / C;
+  a.l_magic = g.L == 1 ? 0u : static_cast<uint32_t>((0x100000000ull + g.L - 1) / g.L);
+  cudaError_t err;
+  if (g.expand)
+    err = g.K <= 8 ? launch_main<8, 256>(g, a, stream) : launch_main<32, 256>(g, a, stream);
+  else
+    err = g.K <= 8 ? launch_main<8, 512>(g, a, stream) : launch_main<32, 512>(g, a, stream);
+  if (err != cudaSuccess) return err;
+  if (g.expand) {
+    layout_expert_scan_kernel<<<(g.E + 31) / 32, kLayoutThreads, 0, stream>>>(a);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  }
-  layout_scan_kernel<<<g.R, kLayoutThreads, scan_smem, stream>>>(a);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  if (ctas > 0) {
-    layout_slot_kernel<<<ctas, kLayoutThreads, slot_smem, stream>>>(a);
+    const size_t smem2 = 2 * sizeof(int32_t) * g.E;
+    if (smem2 > 32 * 1024 &&
+        (err = cudaFuncSetAttribute(layout_expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(smem2))) != cudaSuccess)
+      return err;
+    layout_expand_kernel<<<g.R * C, kLayoutThreads, smem2, stream>>>(a);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
   }
   return cudaSuccess;

@@ -33,7 +33,7 @@ constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) uint8_t g_layout_scratch[kNoAllocScratchBytes];
 
-std::mutex g_scratch_mutex;
+std::mutex g_scratch_mutex;  // guards the per-device address cache
 void* g_scratch_addr[kMaxDevices] = {};
 
 // Device address of this device's scratch array; looked up once per device.

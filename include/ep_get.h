@@ -77,6 +77,11 @@ typedef struct ep_config {
   int32_t num_prologue_sms;        /* SMs for the layout prologue; 0 = automatic;
                                       capped at 64 [P753 "New API"]. Results never
                                       depend on it.                              */
+  int32_t compact_recv;            /* row form only. 0: receive rows at their slots;
+                                      1: each destination's rows packed from row 0 in
+                                      row-block order ([P690] Direct Recv X: the entries
+                                      of row block i start at the exclusive prefix
+                                      recv_psum[d][i-1] of the receive counts)    */
 } ep_config_t;
 
 /* ---- dispatch layout (all device pointers, int32 unless noted) -------------
@@ -111,9 +116,11 @@ typedef struct ep_layout {
 } ep_layout_t;
 
 /* ---- receive buffers (device pointers) -------------------------------------
- * Row form: recv_x/recv_sf rows are indexed d*R*M + slot. Expanded: recv_x and
- * recv_sf rows are indexed exp_region[d] + exp_pos. The sidecars are always row
- * form. Rows no entry fills are left untouched. recv_topk_idx,
+ * Row form: recv_x/recv_sf and the sidecars' rows are indexed d*R*M + slot;
+ * compact (compact_recv = 1): d*R*M + recv_psum[d][rb-1] + slot - rb*M with
+ * rb = slot / M (recv_psum[d][-1] = 0), so destination d's rows are
+ * [d*R*M, d*R*M + sum_s recv_cnt[d][s]). Expanded: recv_x and recv_sf rows are
+ * indexed exp_region[d] + exp_pos; the sidecars stay in the row form. Rows no entry fills are left untouched. recv_topk_idx,
  * recv_topk_weights and recv_src_metadata may be NULL (not written).
  */
 typedef struct ep_recv {
@@ -152,7 +159,7 @@ int ep_get_dispatch_layout(const ep_config_t* cfg, const int64_t* topk_idx,
                            size_t workspace_bytes, void* stream);
 
 /* Size of the fixed scratch array used by ep_get_dispatch_layout_noalloc. */
-#define EP_NOALLOC_SCRATCH_BYTES (4u << 20)
+#define EP_NOALLOC_SCRATCH_BYTES (1u << 20)
 
 /* ep_get_dispatch_layout for callers that cannot allocate device memory (for
  * example plugins of inference engines that are handed only their input and
@@ -190,9 +197,9 @@ int ep_dispatch(const ep_config_t* cfg, const ep_layout_t* layout, const void* x
 
 /* Combine: out[s][t] = bf16_rn(acc), acc = +0 then, for k in lane order over
  * the valid lanes, acc = fma(topk_weights[s][t][k], y[row of lane k], acc),
- * in fp32. y: device bf16 expert outputs in the receive layout (row form
- * [R][R*M][H], or expanded [rows][H]); out: device bf16 [R][T][H]. The result
- * is bitwise reproducible. */
+ * in fp32. y: device bf16 expert outputs in the receive layout (row form or
+ * compact [R][R*M][H], or expanded [rows][H]); out: device bf16 [R][T][H]. The
+ * result is bitwise reproducible. */
 int ep_combine(const ep_config_t* cfg, const ep_layout_t* layout, const uint16_t* y,
                const int64_t* topk_idx, const float* topk_weights, uint16_t* out,
                void* workspace, size_t workspace_bytes, void* stream);

@@ -25,7 +25,8 @@ OK, INVALID, UNSUPPORTED, BAD_TOPK, OVERFLOW = 0, -1, -2, -5, -6
 
 class _Cfg(C.Structure):
     _fields_ = [(n, C.c_int32) for n in
-                ("n_so", "n_su", "E", "K", "T", "M", "H", "x_fp8", "recv_fp8", "expand", "align")]
+                ("n_so", "n_su", "E", "K", "T", "M", "H", "x_fp8", "recv_fp8", "expand", "align",
+                 "compact")]
 
 
 _lib = None
@@ -55,15 +56,15 @@ def lib():
         L.orc_layout.restype = C.c_int
         L.orc_layout.argtypes = [P] * 12
         L.orc_dispatch_token.restype = C.c_int
-        L.orc_dispatch_token.argtypes = [P, C.c_int, C.c_int] + [P] * 15
+        L.orc_dispatch_token.argtypes = [P, C.c_int, C.c_int] + [P] * 16
         L.orc_dispatch.restype = C.c_int
-        L.orc_dispatch.argtypes = [P] * 13
+        L.orc_dispatch.argtypes = [P] * 14
         L.orc_combine_token.restype = None
         L.orc_combine_token.argtypes = [C.c_int, C.c_int, P, P, P]
         L.orc_combine_gathered.restype = None
         L.orc_combine_gathered.argtypes = [C.c_int, C.c_int, C.c_int64, P, P, P, P]
         L.orc_combine.restype = C.c_int
-        L.orc_combine.argtypes = [P] * 8
+        L.orc_combine.argtypes = [P] * 9
         _lib = L
     return _lib
 
@@ -75,7 +76,8 @@ def _p(a):
 def cfg_of(wl) -> _Cfg:
     return _Cfg(wl.n_so, wl.n_su, wl.num_experts, wl.num_topk, wl.num_tokens,
                 wl.num_max_tokens_per_rank, wl.hidden, int(wl.x_dtype == "fp8"),
-                int(wl.recv_dtype == "fp8"), int(bool(wl.expand)), wl.expert_alignment)
+                int(wl.recv_dtype == "fp8"), int(bool(wl.expand)), wl.expert_alignment,
+                int(bool(getattr(wl, "compact", False))))
 
 
 def _np(a, dtype):
@@ -202,7 +204,7 @@ def dispatch_token(wl, lay, s, t, x_row, x_sf_row, idx_tok, w_tok):
     slot = np.ascontiguousarray(lay["slot_map"][s, t], dtype=np.int32)
     pos = np.ascontiguousarray(lay["exp_pos"][s, t], dtype=np.int32) if wl.expand else None
     n = lib().orc_dispatch_token(
-        C.byref(c), s, t, _p(slot), _p(pos), _p(xr), _p(sfr),
+        C.byref(c), s, t, _p(slot), _p(pos), _p(lay["recv_psum"]), _p(xr), _p(sfr),
         _p(np.ascontiguousarray(idx_tok, dtype=np.int64)),
         _p(np.ascontiguousarray(w_tok, dtype=np.float32)), _p(hid), _p(hid_sf), _p(hid_dst),
         _p(hid_row), _p(meta_dst), _p(meta_row), _p(meta_idx), _p(meta_w), _p(meta_md))
@@ -236,7 +238,7 @@ def dispatch(wl, lay, x, x_sf, topk_idx, topk_weights):
     )
     st = lib().orc_dispatch(
         C.byref(c), _p(lay["slot_map"]), _p(lay.get("exp_pos")), _p(lay.get("exp_region")),
-        _p(xa), _p(sfa), _p(_np(topk_idx, np.int64)), _p(_np(topk_weights, np.float32)),
+        _p(lay["recv_psum"]), _p(xa), _p(sfa), _p(_np(topk_idx, np.int64)), _p(_np(topk_weights, np.float32)),
         _p(out["recv_x"]), _p(out["recv_sf"]), _p(out["recv_topk_idx"]),
         _p(out["recv_topk_weights"]), _p(out["recv_src_metadata"]))
     return st, out
@@ -265,9 +267,21 @@ def combine_gathered(lane_rows, y, w):
     return out
 
 
+def recv_rows_of_slots(wl, lay, d, slot):
+    """Receive row (inside the destination's region) of row-form slots: the slot
+    itself, or its compact row (entries packed from row 0 in row-block order)."""
+    if not getattr(wl, "compact", False):
+        return slot
+    M, R = wl.num_max_tokens_per_rank, wl.num_ranks
+    rb = slot // M
+    psum = lay["recv_psum"].astype(np.int64)
+    before = np.where(rb > 0, psum[d, np.maximum(rb - 1, 0)], 0)
+    return before + slot - rb * M
+
+
 def global_rows(wl, lay, topk_idx):
-    """Row of every lane in the receive layout: d*R*M + slot (row form) or
-    exp_region[d] + exp_pos (expanded); -1 for masked lanes. int64 [R, T, K]."""
+    """Row of every lane in the receive layout: d*R*M + row (row form or compact)
+    or exp_region[d] + exp_pos (expanded); -1 for masked lanes. int64 [R, T, K]."""
     idx = _np(topk_idx, np.int64)
     R = wl.num_ranks
     L = wl.num_experts // R
@@ -276,8 +290,9 @@ def global_rows(wl, lay, topk_idx):
         r = lay["exp_region"][d].astype(np.int64) + lay["exp_pos"]
         ok = lay["exp_pos"] >= 0
     else:
-        r = d * (R * wl.num_max_tokens_per_rank) + lay["slot_map"]
-        ok = lay["slot_map"] >= 0
+        slot = lay["slot_map"].astype(np.int64)
+        ok = slot >= 0
+        r = d * (R * wl.num_max_tokens_per_rank) + recv_rows_of_slots(wl, lay, d, np.maximum(slot, 0))
     return np.where(ok & (idx >= 0), r, -1).astype(np.int64)
 
 
@@ -289,6 +304,6 @@ def combine(wl, lay, y, topk_idx, topk_weights):
     ya = _np(y, np.uint16)
     out = np.zeros((R, T, H), np.uint16)
     st = lib().orc_combine(C.byref(c), _p(lay["slot_map"]), _p(lay.get("exp_pos")),
-                           _p(lay.get("exp_region")), _p(ya), _p(_np(topk_idx, np.int64)),
+                           _p(lay.get("exp_region")), _p(lay["recv_psum"]), _p(ya), _p(_np(topk_idx, np.int64)),
                            _p(_np(topk_weights, np.float32)), _p(out))
     return st, out

@@ -52,7 +52,7 @@ namespace {
 
 struct Cfg {
   int32_t n_so, n_su, E, K, T, M, H;
-  int32_t x_fp8, recv_fp8, expand, align;
+  int32_t x_fp8, recv_fp8, expand, align, compact;
 };
 
 constexpr int kOk = 0;
@@ -152,7 +152,21 @@ int check_cfg(const Cfg& c) {
   if (c.E < R || c.E % R != 0 || c.T > c.M || c.align < 1) return kInvalid;
   if ((c.x_fp8 || c.recv_fp8) && c.H % 128 != 0) return kInvalid;
   if (c.x_fp8 && !c.recv_fp8) return kUnsupported;
+  if (c.compact && c.expand) return kUnsupported;
   return kOk;
+}
+
+// Receive row of a row-form slot. Row form: the slot itself. Compact (PR #690,
+// Direct Recv X): a destination's entries are packed from row 0 in row-block
+// order, so the entries of row block rb start after everything the
+// destination receives from row blocks before rb (the exclusive prefix of its
+// per-source receive counts).
+int64_t recv_row(const Cfg& c, int d, int64_t slot, const int32_t* recv_psum) {
+  if (!c.compact) return slot;
+  const int R = ranks(c);
+  const int64_t rb = slot / c.M;
+  const int64_t before = rb == 0 ? 0 : recv_psum[static_cast<int64_t>(d) * R + rb - 1];
+  return before + (slot - rb * c.M);
 }
 
 // Lane validity: -1 is masked; anything else outside [0, E) is an error; in
@@ -182,7 +196,7 @@ extern "C" {
 
 struct orc_cfg {
   int32_t n_so, n_su, E, K, T, M, H;
-  int32_t x_fp8, recv_fp8, expand, align;
+  int32_t x_fp8, recv_fp8, expand, align, compact;
 };
 
 static Cfg to_cfg(const orc_cfg* p) {
@@ -338,14 +352,15 @@ int orc_layout(const orc_cfg* p, const int64_t* topk_idx, int32_t* num_tokens_pe
 //   hid      : the row as received (H bf16 values, or H e4m3 codes)
 //   hid_sf   : its G = H/128 fp32 scales (FP8 receive only)
 //   hid_dst / hid_row : the n_hid (destination, row) pairs that receive the
-//              hidden row; row = slot (row form) or the expanded position
-//              inside the destination's region
-//   meta_dst / meta_row : the n_meta deduplicated (destination, slot) pairs
+//              hidden row; row = slot (row form), its compact row, or the
+//              expanded position inside the destination's region
+//   meta_dst / meta_row : the n_meta deduplicated (destination, row) pairs
 //   meta_idx [K][K] int64, meta_w [K][K] fp32, meta_md [K][2+K] int32: the
 //              sidecar rows written at (meta_dst[i], meta_row[i])
 // Returns n_hid | (n_meta << 8).
 int orc_dispatch_token(const orc_cfg* p, int s, int t, const int32_t* slot_tok,
-                       const int32_t* pos_tok, const void* x_row, const float* x_sf_row,
+                       const int32_t* pos_tok, const int32_t* recv_psum, const void* x_row,
+                       const float* x_sf_row,
                        const int64_t* idx_tok, const float* w_tok, uint8_t* hid, float* hid_sf,
                        int32_t* hid_dst, int64_t* hid_row, int32_t* meta_dst, int64_t* meta_row,
                        int64_t* meta_idx, float* meta_w, int32_t* meta_md) {
@@ -381,13 +396,14 @@ int orc_dispatch_token(const orc_cfg* p, int s, int t, const int32_t* slot_tok,
       ++n_hid;
     }
     if (!first) continue;
+    const int64_t row = recv_row(c, d, slot_tok[k], recv_psum);
     if (!c.expand) {
       hid_dst[n_hid] = d;
-      hid_row[n_hid] = slot_tok[k];
+      hid_row[n_hid] = row;
       ++n_hid;
     }
     meta_dst[n_meta] = d;
-    meta_row[n_meta] = slot_tok[k];
+    meta_row[n_meta] = row;
     int32_t* md = meta_md + static_cast<int64_t>(n_meta) * (2 + K);
     md[0] = s;
     md[1] = t;
@@ -403,14 +419,15 @@ int orc_dispatch_token(const orc_cfg* p, int s, int t, const int32_t* slot_tok,
 }
 
 // Full dispatch into caller-provided receive buffers (only filled rows are
-// written; the rest are left as they are).
+// written; the rest are left as they are). recv_psum is needed for the
+// compact layout only.
 //   recv_x [recv_rows][H] (bf16 or e4m3); recv_sf [recv_rows][G] (FP8 only)
 //   recv_topk_idx [R][R*M][K], recv_topk_weights [R][R*M][K],
 //   recv_src_metadata [R][R*M][2+K]
 // In the row form, destination d's rows start at d*R*M; expanded rows at
 // exp_region[d].
 int orc_dispatch(const orc_cfg* p, const int32_t* slot_map, const int32_t* exp_pos,
-                 const int32_t* exp_region, const void* x, const float* x_sf,
+                 const int32_t* exp_region, const int32_t* recv_psum, const void* x, const float* x_sf,
                  const int64_t* topk_idx, const float* topk_weights, void* recv_x,
                  float* recv_sf, int64_t* recv_topk_idx, float* recv_topk_weights,
                  int32_t* recv_src_metadata) {
@@ -432,7 +449,7 @@ int orc_dispatch(const orc_cfg* p, const int32_t* slot_map, const int32_t* exp_p
       const int64_t tok = static_cast<int64_t>(s) * T + t;
       for (int k = 0; k < K; ++k) lane_valid(c, topk_idx + tok * K, k, &status);
       const int n = orc_dispatch_token(
-          p, s, t, slot_map + tok * K, c.expand ? exp_pos + tok * K : nullptr,
+          p, s, t, slot_map + tok * K, c.expand ? exp_pos + tok * K : nullptr, recv_psum,
           static_cast<const uint8_t*>(x) + tok * H * in_eb, x_sf ? x_sf + tok * G : nullptr,
           topk_idx + tok * K, topk_weights + tok * K, hid.data(), hid_sf.data(), hid_dst.data(),
           hid_row.data(), meta_dst.data(), meta_row.data(), meta_idx.data(), meta_w.data(),
@@ -482,10 +499,10 @@ void orc_combine_gathered(int K, int H, int64_t n, const int64_t* lane_rows, con
   }
 }
 
-// Full combine: y holds the expert outputs in the receive layout (row form:
-// destination d's rows start at d*R*M; expanded: at exp_region[d]).
+// Full combine: y holds the expert outputs in the receive layout (row form or
+// compact: destination d's rows start at d*R*M; expanded: at exp_region[d]).
 int orc_combine(const orc_cfg* p, const int32_t* slot_map, const int32_t* exp_pos,
-                const int32_t* exp_region, const uint16_t* y, const int64_t* topk_idx,
+                const int32_t* exp_region, const int32_t* recv_psum, const uint16_t* y, const int64_t* topk_idx,
                 const float* topk_weights, uint16_t* out) {
   const Cfg c = to_cfg(p);
   int status = check_cfg(c);
@@ -500,9 +517,9 @@ int orc_combine(const orc_cfg* p, const int32_t* slot_map, const int32_t* exp_po
         rows[k] = nullptr;
         if (!lane_valid(c, topk_idx + tok * K, k, &status)) continue;
         const int d = static_cast<int>(topk_idx[tok * K + k]) / L;
-        const int64_t r = c.expand ? static_cast<int64_t>(exp_region[d]) + exp_pos[tok * K + k]
-                                   : d * region_rows + slot_map[tok * K + k];
         if ((c.expand ? exp_pos[tok * K + k] : slot_map[tok * K + k]) < 0) continue;
+        const int64_t r = c.expand ? static_cast<int64_t>(exp_region[d]) + exp_pos[tok * K + k]
+                                   : d * region_rows + recv_row(c, d, slot_map[tok * K + k], recv_psum);
         rows[k] = y + r * H;
       }
       orc_combine_token(K, H, rows.data(), topk_weights + tok * K, out + tok * H);

@@ -87,7 +87,9 @@ def filled_rows(wl, olay, idx):
     L = wl.num_experts // R
     idx = idx.numpy() if hasattr(idx, "numpy") else idx
     d = np.where(idx >= 0, idx // L, 0)
-    side = np.where(olay["slot_map"] >= 0, d * R * M + olay["slot_map"], -1)
+    slot = olay["slot_map"].astype(np.int64)
+    row = oracle.recv_rows_of_slots(wl, olay, d, np.maximum(slot, 0))
+    side = np.where(slot >= 0, d * R * M + row, -1)
     side = np.unique(side[side >= 0])
     return hid, side
 

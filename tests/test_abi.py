@@ -56,14 +56,14 @@ def test_recv_rows_closed_forms(ep):
 
 
 def test_workspace_bytes_closed_form(ep):
-    def expect(R, T, E, expand):
-        NB = -(-T // 256)
-        a = lambda v: (v + 255) // 256 * 256
-        return 256 + 2 * a(4 * R * NB * R) + a(4 * R * NB * E) + (a(4 * R * NB * E) if expand else 0)
-    assert ep.ep_workspace_bytes(cfg(ep)) == expect(16, 4096, 256, False)
-    assert ep.ep_workspace_bytes(cfg(ep, expand=1)) == expect(16, 4096, 256, True)
+    # a 256-byte header (device error bits, the layout kernel's arrival counter)
+    # plus, expanded, the per-(source, expert) cross-source offsets
+    def expect(R, E, expand):
+        return 256 + ((4 * R * E + 255) // 256 * 256 if expand else 0)
+    assert ep.ep_workspace_bytes(cfg(ep)) == expect(16, 256, False)
+    assert ep.ep_workspace_bytes(cfg(ep, expand=1)) == expect(16, 256, True)
     assert ep.ep_workspace_bytes(cfg(ep, num_scaleup_ranks=64, num_experts=512, num_tokens=513,
-                                     num_max_tokens_per_rank=600, expand=1)) == expect(64, 513, 512, True)
+                                     num_max_tokens_per_rank=600, expand=1)) == expect(64, 512, True)
     assert ep.ep_workspace_bytes(cfg(ep, num_tokens=0)) == 256
 
 
@@ -80,6 +80,8 @@ def test_workspace_bytes_closed_form(ep):
     (dict(num_experts=8192), -2),
     (dict(expert_alignment=0), -1),
     (dict(x_dtype=7), -1),
+    (dict(compact_recv=2), -1),
+    (dict(compact_recv=1, expand=1), -2),     # expanded rows are packed already
 ])
 def test_invalid_configs_are_rejected_before_any_launch(ep, bad, code):
     c = cfg(ep, **bad)

@@ -219,3 +219,64 @@ def test_combine_is_a_fused_chain_in_lane_order(orc):
     assert out.tolist() == [0x3F81]
     rev = orc.combine_token([np.array([v], np.uint16) for v in y[::-1]], w[::-1].copy())
     assert rev.tolist() == [0x3F80]
+
+
+# ---- compact receive rows (PR #690, Direct Recv X) ---------------------------
+
+def _row_block(wl, s):
+    return s if wl.n_so == 1 else (s % wl.n_su) * wl.n_so + s // wl.n_su
+
+
+@pytest.mark.parametrize("name", ["direct_zipf_compact", "hybrid_compact"])
+def test_compact_rows_pack_each_destination_in_row_block_order(orc, name):
+    """Each destination's entries, sorted by (source row block, token), occupy
+    rows 0, 1, 2, ... of its region: the compact receive layout."""
+    wl = W.PARITY[name].replace(num_tokens=23, num_max_tokens_per_rank=29, hidden=128)
+    idx, w = W.routing(wl)
+    x, _ = W.hidden(wl)
+    st, lay = orc.layout(wl, idx)
+    assert st == 0
+    R, T, K = wl.num_ranks, wl.num_tokens, wl.num_topk
+    L = wl.num_experts // R
+    idx_np = idx.numpy()
+    xb = _bits(x)
+    expect = {}
+    for d in range(R):
+        ents = sorted({(_row_block(wl, s), t, s) for s in range(R) for t in range(T)
+                       for e in idx_np[s, t] if e >= 0 and e // L == d})
+        for i, (_, t, s) in enumerate(ents):
+            expect[(s, t, d)] = i
+        assert len(ents) == lay["recv_cnt"][d].sum()
+    got = {}
+    for s in range(R):
+        for t in range(T):
+            o = orc.dispatch_token(wl, lay, s, t, xb[s, t], None, idx_np[s, t], w.numpy()[s, t])
+            for dd, r in zip(o["meta_dst"], o["meta_row"]):
+                got[(s, t, int(dd))] = int(r)
+            assert sorted(zip(o["hid_dst"].tolist(), o["hid_row"].tolist())) == \
+                sorted(zip(o["meta_dst"].tolist(), o["meta_row"].tolist()))
+    assert got == expect
+
+
+@pytest.mark.parametrize("name", ["direct_zipf_compact", "hybrid_compact"])
+def test_compact_and_row_form_give_the_same_combine(orc, name):
+    wl = W.PARITY[name].replace(num_tokens=40, num_max_tokens_per_rank=48, hidden=256)
+    idx, w = W.routing(wl)
+    x, _ = W.hidden(wl)
+    outs = []
+    for compact in (True, False):
+        v = wl.replace(compact=compact)
+        _, lay = orc.layout(v, idx)
+        st, rec = orc.dispatch(v, lay, x, None, idx, w)
+        assert st == 0
+        st, out = orc.combine(v, lay, rec["recv_x"], idx, w)
+        assert st == 0
+        outs.append(out)
+        if compact:
+            # filled rows of destination d are exactly the first sum_s recv_cnt[d][s]
+            R, M = v.num_ranks, v.num_max_tokens_per_rank
+            md = rec["recv_src_metadata"].reshape(R, R * M, -1)
+            for d in range(R):
+                n = int(lay["recv_cnt"][d].sum())
+                assert np.all(md[d, :n, 0] >= 0) and not md[d, n:].any()
+    assert np.array_equal(outs[0], outs[1])

@@ -30,7 +30,7 @@ def test_noalloc_layout_matches_the_workspace_entry_point(name):
     ref = GpuRun(wl, idx, w, x, sf).layout()
     assert ref.status() == ep.EP_OK
     expect = ref.layout_np()
-    assert ep.ep_workspace_bytes(ref.cfg) <= 4 << 20
+    assert ep.ep_workspace_bytes(ref.cfg) <= 1 << 20
     lay = ep.alloc_layout(ref.cfg, ref.dev)
     for _ in range(2):  # two calls in a row share the library's scratch
         _poison(lay)
@@ -47,9 +47,15 @@ def test_noalloc_layout_matches_the_workspace_entry_point(name):
 
 
 def test_noalloc_rejects_configs_beyond_its_scratch():
-    cfg = ep.Config(1, 64, 4096, 8, 4096, 4096, 128)
-    assert ep.ep_workspace_bytes(cfg) > 4 << 20
+    # expanded: the scratch holds one int32 per (source rank, expert) after a
+    # 256-byte header; 64 ranks x 4096 experts needs 1 MiB + 256 bytes
+    cfg = ep.Config(1, 64, 4096, 8, 16, 16, 128, expand=1)
+    assert ep.ep_workspace_bytes(cfg) > 1 << 20
     lay = ep.alloc_layout(ep.Config(1, 1, 1, 1, 0, 1, 8), "cuda")  # never written
     with pytest.raises(ep.EpError) as e:
         ep.ep_get_dispatch_layout_noalloc(cfg, torch.empty(0, dtype=torch.int64, device="cuda"), lay)
     assert e.value.status == ep.EP_ERR_WORKSPACE
+    bad = ep.Config(1, 16, 250, 8, 16, 16, 128)  # experts not a multiple of the ranks
+    with pytest.raises(ep.EpError) as e:
+        ep.ep_get_dispatch_layout_noalloc(bad, torch.empty(0, dtype=torch.int64, device="cuda"), lay)
+    assert e.value.status == ep.EP_ERR_INVALID_ARG

@@ -46,6 +46,7 @@ class Workload:
     recv_dtype: str = "bf16"      # "bf16" | "fp8" (fused cast when x is bf16)
     expand: bool = False
     expert_alignment: int = 1
+    compact: bool = False         # compact receive rows (row form only)
     routing: str = "gauss"        # "gauss" | "zipf" | "hot"
     zipf_s: float = 1.1
     mask_frac: float = 0.0
@@ -95,6 +96,11 @@ PARITY = {
         name="dsv3_fp8_precast", x_dtype="fp8", num_tokens=288, num_max_tokens_per_rank=288),
     "hybrid_rowform": WORKLOADS["hybrid_rowform"].replace(num_tokens=300, num_max_tokens_per_rank=300),
     "expanded": WORKLOADS["expanded"].replace(num_tokens=100, num_max_tokens_per_rank=100),
+    # compact receive rows (each destination's rows packed from row 0)
+    "direct_zipf_compact": WORKLOADS["direct_zipf"].replace(
+        name="direct_zipf_compact", compact=True, num_tokens=300, num_max_tokens_per_rank=320),
+    "hybrid_compact": WORKLOADS["hybrid_rowform"].replace(
+        name="hybrid_compact", compact=True, num_tokens=300, num_max_tokens_per_rank=300),
 }
 
 
