@@ -46,6 +46,12 @@ def parse():
                    help="override tokens per rank (small cases for profiling only)")
     p.add_argument("--compact", action="store_true",
                    help="compact receive rows (each destination packed from row 0)")
+    p.add_argument("--align", type=int, default=0, help="expert_alignment of the expanded layout")
+    p.add_argument("--zero-padding", action="store_true", help="zero the alignment padding rows")
+    p.add_argument("--cached", action="store_true",
+                   help="time dispatch + combine only, replaying a layout computed once")
+    p.add_argument("--compare-sort", action="store_true",
+                   help="time the deterministic dispatch against atomic slots + post-hoc sort")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline sample")
@@ -58,6 +64,10 @@ def workload(args):
         wl = wl.replace(num_tokens=args.tokens, num_max_tokens_per_rank=max(args.tokens, 1))
     if args.compact:
         wl = wl.replace(compact=True)
+    if args.align:
+        wl = wl.replace(expert_alignment=args.align)
+    if args.zero_padding:
+        wl = wl.replace(zero_padding=True)
     return wl
 
 
@@ -66,6 +76,8 @@ def describe(wl) -> str:
         f"hybrid row form {wl.n_so}x{wl.n_su}" if wl.n_so > 1 else "direct row form")
     if wl.compact:
         lay += ", compact receive rows"
+    if wl.expand and wl.expert_alignment > 1:
+        lay += f", blocks aligned to {wl.expert_alignment}" + (" with zeroed padding" if wl.zero_padding else "")
     cast = {("bf16", "fp8"): "bf16 x cast to fp8-e4m3 inside dispatch (fp32 scale per 128 columns)",
             ("fp8", "fp8"): "pre-cast fp8-e4m3 x + fp32 scales",
             ("bf16", "bf16"): "bf16 rows"}[(wl.x_dtype, wl.recv_dtype)]
@@ -84,9 +96,10 @@ def peaks():
 
 # ---- algorithmic bytes (only what the method must move) ---------------------
 
-def algorithmic_bytes(wl, ntpr, valid_lanes, tokens_with_lane):
+def algorithmic_bytes(wl, ntpr, valid_lanes, tokens_with_lane, pad_rows=0):
     """Bytes per launch of each phase. ntpr: total deduplicated rows; valid_lanes:
-    lanes with an expert; tokens_with_lane: source tokens with >= 1 valid lane."""
+    lanes with an expert; tokens_with_lane: source tokens with >= 1 valid lane;
+    pad_rows: alignment padding rows dispatch zeroes (expanded, zero padding)."""
     R, T, K, H = wl.num_ranks, wl.num_tokens, wl.num_topk, wl.hidden
     G = H // 128
     n_tok = R * T
@@ -100,6 +113,7 @@ def algorithmic_bytes(wl, ntpr, valid_lanes, tokens_with_lane):
                 + (tokens_with_lane * G * 4 if wl.x_dtype == "fp8" else 0)
                 + hid_rows * H * eb_out                            # hidden rows written
                 + (hid_rows * G * 4 if wl.recv_dtype == "fp8" else 0)
+                + pad_rows * (H * eb_out + (G * 4 if wl.recv_dtype == "fp8" else 0))  # zeroed padding
                 + ntpr * (K * 8 + K * 4 + (2 + K) * 4)             # sidecar rows
                 + n_tok * K * (8 + 4 + 4))                         # topk_idx, weights, slots read
     combine = (hid_rows * H * 2                                    # each expert-output row once
@@ -229,13 +243,16 @@ def native(args):
 
     def step(e=None):
         if e: e[0].record(stream)
-        ep.ep_get_dispatch_layout(cfg, idx, lay, ws, stream)
+        if not args.cached:
+            ep.ep_get_dispatch_layout(cfg, idx, lay, ws, stream)
         if e: e[1].record(stream)
         ep.ep_dispatch(cfg, lay, x, sf, idx, w, recv, ws, stream)
         if e: e[2].record(stream)
         ep.ep_combine(cfg, lay, y, idx, w, out, ws, stream)
         if e: e[3].record(stream)
 
+    if args.cached:  # the stored layout every timed step replays
+        ep.ep_get_dispatch_layout(cfg, idx, lay, ws, stream)
     for _ in range(max(args.warmup, 0)):
         step()
     torch.cuda.synchronize(dev)
@@ -265,7 +282,8 @@ def native(args):
     valid = idx_h >= 0
     valid_lanes = int(valid.sum().item())
     tokens_with_lane = int(valid.any(-1).sum().item())
-    abytes = algorithmic_bytes(wl, ntpr, valid_lanes, tokens_with_lane)
+    pad_rows = (int(lay.exp_region[-1].item()) - valid_lanes) if (wl.expand and wl.zero_padding) else 0
+    abytes = algorithmic_bytes(wl, ntpr, valid_lanes, tokens_with_lane, pad_rows)
     peak, peak_kind = peaks()
     gbs = {k: abytes[k] / (phase_ms[k] * 1e-3) / 1e9 for k in abytes}
     dominant = max(("dispatch", "combine"), key=lambda k: phase_ms[k])
@@ -290,7 +308,8 @@ def native(args):
                   if wl.recv_dtype == "fp8" and wl.x_dtype == "bf16" else
                   f"{wl.x_dtype} x -> {wl.recv_dtype} recv, fp32 combine accumulate"),
         "data": "synthetic (seeded routing and activations)",
-        "config": {"workload": describe(wl), "tokens_per_step": R * T, "dedup_rows": ntpr,
+        "config": {"workload": describe(wl) + (" (cached: layout replayed, not timed)" if args.cached else ""),
+                   "tokens_per_step": R * T, "dedup_rows": ntpr,
                    "l2": "inputs larger than L2 between steps (no flush)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "phases": {
@@ -300,7 +319,7 @@ def native(args):
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": gbs[dominant] / peak, "traffic": ncu_traffic(dominant, wl, R * T)},
         "clocks": clocks.summary(),
-        "gpu_launches": args.steps * (5 if T > 0 else 1),
+        "gpu_launches": args.steps * launches_per_step(wl, args.cached),
     }
     if e2e is not None:
         line["e2e"] = e2e
@@ -313,52 +332,80 @@ def native(args):
         dist.destroy_process_group()
 
 
+def launches_per_step(wl, cached=False):
+    """Kernels of this library one step launches: the layout (one kernel, three
+    when expanded), dispatch and combine."""
+    layout = 0 if cached else (3 if wl.expand else 1)
+    return layout + (2 if wl.num_tokens > 0 else 0)
+
+
 def end_to_end(ep, cfg, wl, idx_h, w_h, x_h, sf_h, lay, recv, y, identity, ws, stream, dev, args,
                world):
-    """The same step through the public API from pinned host buffers: host->device
-    copies of the step's inputs and the device->host copy of its output are inside
-    the timed region."""
+    """The same step through the public API from pinned host buffers: every step
+    copies its inputs host->device and its output device->host inside the timed
+    region. Copies run on their own streams, double-buffered, so step i+1's
+    inputs and step i-1's output move while step i computes."""
     R, T, H = wl.num_ranks, wl.num_tokens, wl.hidden
     hx = x_h.pin_memory()
     hidx = idx_h.pin_memory()
     hw = w_h.pin_memory()
     hsf = None if sf_h is None else sf_h.pin_memory()
-    hout = torch.empty(R, T, H, dtype=torch.bfloat16).pin_memory()
-    dx = torch.empty_like(hx, device=dev)
-    didx = torch.empty_like(hidx, device=dev)
-    dw = torch.empty_like(hw, device=dev)
-    dsf = None if hsf is None else torch.empty_like(hsf, device=dev)
-    dout = torch.empty(R, T, H, dtype=torch.bfloat16, device=dev)
+    nb = 2
+    hout = [torch.empty(R, T, H, dtype=torch.bfloat16).pin_memory() for _ in range(nb)]
+    dx = [torch.empty_like(hx, device=dev) for _ in range(nb)]
+    didx = [torch.empty_like(hidx, device=dev) for _ in range(nb)]
+    dw = [torch.empty_like(hw, device=dev) for _ in range(nb)]
+    dsf = [None if hsf is None else torch.empty_like(hsf, device=dev) for _ in range(nb)]
+    dout = [torch.empty(R, T, H, dtype=torch.bfloat16, device=dev) for _ in range(nb)]
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()
+    in_done = [ev() for _ in range(nb)]
+    comp_done = [ev() for _ in range(nb)]
+    out_done = [ev() for _ in range(nb)]
     steps = max(3, min(args.steps, 10))
 
-    def step():
-        dx.copy_(hx, non_blocking=True)
-        didx.copy_(hidx, non_blocking=True)
-        dw.copy_(hw, non_blocking=True)
-        if dsf is not None:
-            dsf.copy_(hsf, non_blocking=True)
-        ep.ep_get_dispatch_layout(cfg, didx, lay, ws, stream)
-        ep.ep_dispatch(cfg, lay, dx, dsf, didx, dw, recv, ws, stream)
-        ep.ep_combine(cfg, lay, recv.recv_x if identity else y, didx, dw, dout, ws, stream)
-        hout.copy_(dout, non_blocking=True)
+    def run(n):
+        for i in range(n):
+            b = i % nb
+            if i >= nb:
+                s_in.wait_event(comp_done[b])      # step i-2 no longer reads buffer b
+            with torch.cuda.stream(s_in):
+                dx[b].copy_(hx, non_blocking=True)
+                didx[b].copy_(hidx, non_blocking=True)
+                dw[b].copy_(hw, non_blocking=True)
+                if dsf[b] is not None:
+                    dsf[b].copy_(hsf, non_blocking=True)
+                in_done[b].record(s_in)
+            stream.wait_event(in_done[b])
+            if i >= nb:
+                stream.wait_event(out_done[b])     # step i-2's output has left dout[b]
+            ep.ep_get_dispatch_layout(cfg, didx[b], lay, ws, stream)
+            ep.ep_dispatch(cfg, lay, dx[b], dsf[b], didx[b], dw[b], recv, ws, stream)
+            ep.ep_combine(cfg, lay, recv.recv_x if identity else y, didx[b], dw[b], dout[b], ws, stream)
+            comp_done[b].record(stream)
+            s_out.wait_event(comp_done[b])
+            with torch.cuda.stream(s_out):
+                hout[b].copy_(dout[b], non_blocking=True)
+                out_done[b].record(s_out)
+        stream.wait_stream(s_out)
 
-    for _ in range(2):
-        step()
+    run(2)
     torch.cuda.synchronize(dev)
     barrier(world)
     a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
+    b_ = torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    for _ in range(steps):
-        step()
-    b.record(stream)
+    s_in.wait_stream(stream)
+    run(steps)
+    b_.record(stream)
     torch.cuda.synchronize(dev)
-    ms = max_over_ranks(world, a.elapsed_time(b)) / steps
+    ms = max_over_ranks(world, a.elapsed_time(b_)) / steps
     h2d = hx.numel() * hx.element_size() + hidx.numel() * 8 + hw.numel() * 4 + \
         (0 if hsf is None else hsf.numel() * 4)
-    d2h = hout.numel() * 2
-    return {"value": world * R * T / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    d2h = hout[0].numel() * 2
+    return {"value": whole_job_rate(world, R * T, ms * steps, steps), "unit": "tokens/s",
+            "ms_per_step": ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "pipeline": "double-buffered host copies on two copy streams"}
 
 
 def ncu_traffic(kernel, wl, n_tok):
@@ -476,10 +523,57 @@ def reference(args):
     print(json.dumps(line), flush=True)
 
 
+def compare_sort(args):
+    """PR #753's comparison on one GPU: layout + deterministic dispatch against
+    atomic-slot dispatch + post-hoc sort (same rows, same sidecars)."""
+    import combine_ep_get_02_gb300 as ep
+    dev = torch.device("cuda", 0)
+    wl = workload(args)
+    cfg = ep.config_of(wl)
+    idx_h, w_h = W.routing(wl)
+    x_h, sf_h = W.hidden(wl)
+    idx, w, x = idx_h.to(dev), w_h.to(dev), x_h.to(dev)
+    sf = None if sf_h is None else sf_h.to(dev)
+    ws = ep.alloc_workspace(cfg, dev)
+    lay = ep.alloc_layout(cfg, dev)
+    recv = ep.alloc_recv(cfg, dev, zero=True)
+    racy = ep.alloc_recv(cfg, dev, zero=True)
+    srt = ep.alloc_recv(cfg, dev, zero=True)
+    counters = torch.zeros(wl.num_ranks, wl.num_ranks, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(fns, steps):
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(fns) + 1)] for _ in range(steps)]
+        for _ in range(max(args.warmup, 1)):
+            for f in fns:
+                f()
+        torch.cuda.synchronize(dev)
+        for e in evs:
+            e[0].record(stream)
+            for j, f in enumerate(fns):
+                f()
+                e[j + 1].record(stream)
+        torch.cuda.synchronize(dev)
+        return [statistics.mean(e[j].elapsed_time(e[j + 1]) * 1e3 for e in evs) for j in range(len(fns))]
+
+    det = timed([lambda: ep.ep_get_dispatch_layout(cfg, idx, lay, ws, stream),
+                 lambda: ep.ep_dispatch(cfg, lay, x, sf, idx, w, recv, ws, stream)], args.steps)
+    old = timed([lambda: ep.ep_dispatch_atomic(cfg, x, sf, idx, w, racy, counters, stream),
+                 lambda: ep.ep_deterministic_sort(cfg, racy, counters, srt, stream)], args.steps)
+    same = all(torch.equal(getattr(recv, f).view(torch.uint8), getattr(srt, f).view(torch.uint8))
+               for f in ("recv_x", "recv_topk_idx", "recv_topk_weights", "recv_src_metadata"))
+    print(json.dumps({"mode": "sort_comparison", "workload": describe(wl), "steps": args.steps,
+                      "deterministic_us": {"layout": det[0], "dispatch": det[1], "total": sum(det)},
+                      "atomic_sort_us": {"atomic_dispatch": old[0], "sort": old[1], "total": sum(old)},
+                      "speedup": sum(old) / sum(det), "identical_after_sort": same}), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         reference(args)
+    elif args.compare_sort:
+        compare_sort(args)
     else:
         native(args)
 

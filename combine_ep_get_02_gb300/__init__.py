@@ -27,6 +27,7 @@ EP_DTYPE_BF16, EP_DTYPE_FP8_E4M3 = 0, 1
 __all__ = [
     "Config", "Layout", "Recv", "EpError", "lib", "ep_workspace_bytes", "ep_recv_rows",
     "ep_workspace_init", "ep_get_dispatch_layout", "ep_get_dispatch_layout_noalloc", "ep_dispatch", "ep_combine", "ep_check_error",
+    "ep_dispatch_atomic", "ep_deterministic_sort",
     "ep_status_string", "ep_diag_e4m3_of_bits", "ep_diag_bf16_of_bits", "alloc_layout", "alloc_recv",
     "alloc_workspace", "config_of",
 ]
@@ -42,7 +43,7 @@ class _Config(C.Structure):
     _fields_ = [(n, C.c_int32) for n in (
         "num_scaleout_ranks", "num_scaleup_ranks", "num_experts", "num_topk", "num_tokens",
         "num_max_tokens_per_rank", "hidden", "x_dtype", "recv_dtype", "expand", "expert_alignment",
-        "num_sms", "num_prologue_sms", "compact_recv")]
+        "num_sms", "num_prologue_sms", "compact_recv", "zero_padding")]
 
 
 class _Layout(C.Structure):
@@ -73,6 +74,7 @@ class Config:
     num_sms: int = 0
     num_prologue_sms: int = 0
     compact_recv: int = 0
+    zero_padding: int = 0
 
     @property
     def num_ranks(self) -> int:
@@ -89,7 +91,8 @@ def config_of(wl, **over) -> Config:
                EP_DTYPE_FP8_E4M3 if wl.x_dtype == "fp8" else EP_DTYPE_BF16,
                EP_DTYPE_FP8_E4M3 if wl.recv_dtype == "fp8" else EP_DTYPE_BF16,
                int(bool(wl.expand)), wl.expert_alignment,
-               compact_recv=int(bool(getattr(wl, "compact", False))))
+               compact_recv=int(bool(getattr(wl, "compact", False))),
+               zero_padding=int(bool(getattr(wl, "zero_padding", False))))
     return dataclasses.replace(c, **over)
 
 
@@ -117,6 +120,10 @@ def lib():
         L.ep_get_dispatch_layout_noalloc.argtypes = [P, P, P, P]
         L.ep_dispatch.restype = I
         L.ep_dispatch.argtypes = [P, P, P, P, P, P, P, P, C.c_size_t, P]
+        L.ep_dispatch_atomic.restype = I
+        L.ep_dispatch_atomic.argtypes = [P, P, P, P, P, P, P, P]
+        L.ep_deterministic_sort.restype = I
+        L.ep_deterministic_sort.argtypes = [P, P, P, P, P]
         L.ep_combine.restype = I
         L.ep_combine.argtypes = [P, P, P, P, P, P, P, C.c_size_t, P]
         L.ep_check_error.restype = I
@@ -254,6 +261,22 @@ def ep_dispatch(cfg: Config, layout: Layout, x: torch.Tensor, x_sf, topk_idx: to
     _check(lib().ep_dispatch(C.byref(c), C.byref(l), _ptr(x), _ptr(x_sf), _ptr(topk_idx),
                              _ptr(topk_weights), C.byref(r), _ptr(ws), ws.numel(), _stream(stream)),
            "ep_dispatch")
+
+
+def ep_dispatch_atomic(cfg: Config, x: torch.Tensor, x_sf, topk_idx: torch.Tensor,
+                       topk_weights: torch.Tensor, recv: Recv, send_counters: torch.Tensor, stream=None):
+    """Comparison path: dispatch with racing atomicAdd slots (no layout)."""
+    c, r = cfg._c(), recv._c()
+    _check(lib().ep_dispatch_atomic(C.byref(c), _ptr(x), _ptr(x_sf), _ptr(topk_idx), _ptr(topk_weights),
+                                    C.byref(r), _ptr(send_counters), _stream(stream)), "ep_dispatch_atomic")
+
+
+def ep_deterministic_sort(cfg: Config, recv: Recv, send_counters: torch.Tensor, sorted_recv: Recv,
+                          stream=None):
+    """Comparison path: sort each received segment by source token into sorted_recv."""
+    c, r, o = cfg._c(), recv._c(), sorted_recv._c()
+    _check(lib().ep_deterministic_sort(C.byref(c), C.byref(r), _ptr(send_counters), C.byref(o),
+                                       _stream(stream)), "ep_deterministic_sort")
 
 
 def ep_combine(cfg: Config, layout: Layout, y: torch.Tensor, topk_idx: torch.Tensor,

@@ -74,6 +74,8 @@ int make_geometry(const ep_config_t* c, Geometry* g) {
   if (c->num_sms < 0 || c->num_prologue_sms < 0) return EP_ERR_INVALID_ARG;
   if (c->compact_recv != 0 && c->compact_recv != 1) return EP_ERR_INVALID_ARG;
   if (c->compact_recv && c->expand) return EP_ERR_UNSUPPORTED;  // expanded rows are packed already
+  if (c->zero_padding != 0 && c->zero_padding != 1) return EP_ERR_INVALID_ARG;
+  if (c->zero_padding && !c->expand) return EP_ERR_UNSUPPORTED;  // only expanded blocks are padded
   // 32-bit row indices: rows of one region, lanes, and expanded rows must fit
   const int64_t region_rows = R * c->num_max_tokens_per_rank;
   const int64_t lanes = R * c->num_tokens * c->num_topk;
@@ -95,6 +97,7 @@ int make_geometry(const ep_config_t* c, Geometry* g) {
   g->expand = c->expand;
   g->align = c->expert_alignment;
   g->compact = c->compact_recv;
+  g->zero_padding = c->zero_padding;
   g->region_rows = region_rows;
   g->num_tokens = R * c->num_tokens;
   return EP_OK;
@@ -223,6 +226,8 @@ int ep_dispatch(const ep_config_t* cfg, const ep_layout_t* layout, const void* x
   if (g.expand && (layout->exp_pos == nullptr || layout->exp_region == nullptr))
     return EP_ERR_INVALID_ARG;
   if (g.compact && layout->recv_psum == nullptr) return EP_ERR_INVALID_ARG;
+  if (g.zero_padding && (layout->exp_cnt == nullptr || layout->exp_base == nullptr))
+    return EP_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(recv->recv_x, 16) || !aligned(topk_idx, 8) ||
       !aligned(topk_weights, 4) || !aligned(x_sf, 4) || !aligned(recv->recv_sf, 4) ||
       !aligned(recv->recv_topk_idx, 8) || !aligned(recv->recv_topk_weights, 4) ||
@@ -241,6 +246,8 @@ int ep_dispatch(const ep_config_t* cfg, const ep_layout_t* layout, const void* x
   a.exp_pos = layout->exp_pos;
   a.exp_region = layout->exp_region;
   a.recv_psum = layout->recv_psum;
+  a.exp_cnt = layout->exp_cnt;
+  a.exp_base = layout->exp_base;
   a.recv_x = static_cast<uint8_t*>(recv->recv_x);
   a.recv_sf = recv->recv_sf;
   a.recv_idx = recv->recv_topk_idx;
@@ -255,6 +262,7 @@ int ep_dispatch(const ep_config_t* cfg, const ep_layout_t* layout, const void* x
   a.G = g.G;
   a.M = g.M;
   a.compact = g.compact;
+  a.zero_padding = g.zero_padding;
   a.region_rows = g.region_rows;
   a.num_tokens = g.num_tokens;
   a.in_row_bytes = g.H * (g.x_fp8 ? 1 : 2);
@@ -301,6 +309,95 @@ int ep_combine(const ep_config_t* cfg, const ep_layout_t* layout, const uint16_t
   a.region_rows = g.region_rows;
   a.num_tokens = g.num_tokens;
   return cuda_status(launch_combine(g, a, sms, static_cast<cudaStream_t>(stream)));
+}
+
+int ep_dispatch_atomic(const ep_config_t* cfg, const void* x, const float* x_sf,
+                       const int64_t* topk_idx, const float* topk_weights, const ep_recv_t* recv,
+                       int32_t* send_counters, void* stream) {
+  Geometry g;
+  int st = make_geometry(cfg, &g);
+  if (st != EP_OK) return st;
+  if (g.expand || g.compact || g.zero_padding) return EP_ERR_UNSUPPORTED;
+  if (recv == nullptr || send_counters == nullptr) return EP_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(send_counters, 0, sizeof(int32_t) * g.R * g.R, s) != cudaSuccess) return EP_ERR_CUDA;
+  if (g.num_tokens == 0) return EP_OK;
+  if (x == nullptr || topk_idx == nullptr || topk_weights == nullptr || recv->recv_x == nullptr)
+    return EP_ERR_INVALID_ARG;
+  if (g.x_fp8 != (x_sf != nullptr) || (g.recv_fp8 && recv->recv_sf == nullptr)) return EP_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(recv->recv_x, 16) || !aligned(topk_idx, 8) ||
+      !aligned(topk_weights, 4) || !aligned(send_counters, 4))
+    return EP_ERR_INVALID_ARG;
+  if (recv->recv_x_rows < static_cast<int64_t>(g.R) * g.region_rows) return EP_ERR_INVALID_ARG;
+  const int sms = sms_or_all(cfg->num_sms);
+  if (sms < 0) return EP_ERR_CUDA;
+  DispatchArgs a = {};
+  a.x = static_cast<const uint8_t*>(x);
+  a.x_sf = x_sf;
+  a.topk_idx = topk_idx;
+  a.topk_w = topk_weights;
+  a.send_counters = send_counters;
+  a.recv_x = static_cast<uint8_t*>(recv->recv_x);
+  a.recv_sf = recv->recv_sf;
+  a.recv_idx = recv->recv_topk_idx;
+  a.recv_w = recv->recv_topk_weights;
+  a.recv_md = recv->recv_src_metadata;
+  a.R = g.R;
+  a.E = g.E;
+  a.L = g.L;
+  a.K = g.K;
+  a.T = g.T;
+  a.H = g.H;
+  a.G = g.G;
+  a.M = g.M;
+  a.n_so = g.n_so;
+  a.n_su = g.n_su;
+  a.region_rows = g.region_rows;
+  a.num_tokens = g.num_tokens;
+  a.in_row_bytes = g.H * (g.x_fp8 ? 1 : 2);
+  a.out_row_bytes = g.H * (g.recv_fp8 ? 1 : 2);
+  return cuda_status(launch_dispatch_atomic(g, a, sms, s));
+}
+
+int ep_deterministic_sort(const ep_config_t* cfg, const ep_recv_t* recv,
+                          const int32_t* send_counters, const ep_recv_t* sorted, void* stream) {
+  Geometry g;
+  int st = make_geometry(cfg, &g);
+  if (st != EP_OK) return st;
+  if (g.expand || g.compact) return EP_ERR_UNSUPPORTED;
+  if (g.M > kMaxSortRows) return EP_ERR_UNSUPPORTED;
+  if (recv == nullptr || sorted == nullptr || send_counters == nullptr) return EP_ERR_INVALID_ARG;
+  const ep_recv_t* bufs[2] = {recv, sorted};
+  for (const ep_recv_t* r : bufs) {
+    if (r->recv_x == nullptr || r->recv_topk_idx == nullptr || r->recv_topk_weights == nullptr ||
+        r->recv_src_metadata == nullptr || (g.recv_fp8 && r->recv_sf == nullptr))
+      return EP_ERR_INVALID_ARG;
+    if (!aligned(r->recv_x, 16) || !aligned(r->recv_topk_idx, 8) || !aligned(r->recv_sf, 4) ||
+        !aligned(r->recv_topk_weights, 4) || !aligned(r->recv_src_metadata, 4))
+      return EP_ERR_INVALID_ARG;
+    if (r->recv_x_rows < static_cast<int64_t>(g.R) * g.region_rows) return EP_ERR_INVALID_ARG;
+  }
+  SortArgs a;
+  a.in_x = static_cast<const uint8_t*>(recv->recv_x);
+  a.in_sf = g.recv_fp8 ? recv->recv_sf : nullptr;
+  a.in_idx = recv->recv_topk_idx;
+  a.in_w = recv->recv_topk_weights;
+  a.in_md = recv->recv_src_metadata;
+  a.out_x = static_cast<uint8_t*>(sorted->recv_x);
+  a.out_sf = sorted->recv_sf;
+  a.out_idx = sorted->recv_topk_idx;
+  a.out_w = sorted->recv_topk_weights;
+  a.out_md = sorted->recv_src_metadata;
+  a.send_counters = send_counters;
+  a.R = g.R;
+  a.K = g.K;
+  a.M = g.M;
+  a.G = g.G;
+  a.n_so = g.n_so;
+  a.n_su = g.n_su;
+  a.region_rows = g.region_rows;
+  a.row_bytes = g.H * (g.recv_fp8 ? 1 : 2);
+  return cuda_status(launch_sort(g, a, static_cast<cudaStream_t>(stream)));
 }
 
 int ep_check_error(void* workspace, void* stream) {

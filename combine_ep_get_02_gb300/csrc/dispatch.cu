@@ -29,9 +29,13 @@ struct TokenLanes {
 };
 
 // Lane k < K: the token's k-th top-k lane. Invalid lanes get a distinct
-// negative d so that they never group with anything.
+// negative d so that they never group with anything. With `atomic` (the
+// prior-art comparison path) there is no layout: the first lane to each
+// destination takes the next row of the source's block with an atomicAdd on
+// the (source, destination) counter, so the order inside a block depends on
+// which warp gets there first (PR #753, Motivation).
 __device__ __forceinline__ TokenLanes load_lanes(const DispatchArgs& a, int64_t tok, int lane,
-                                                 bool expand) {
+                                                 bool expand, bool atomic = false) {
   TokenLanes L;
   L.e = -1;
   L.slot = -1;
@@ -40,21 +44,29 @@ __device__ __forceinline__ TokenLanes load_lanes(const DispatchArgs& a, int64_t 
   if (lane < a.K) {
     const int64_t i = tok * a.K + lane;
     const int64_t e = a.topk_idx[i];
-    L.slot = a.slot_map[i];
+    if (!atomic) L.slot = a.slot_map[i];
     L.w = a.topk_w[i];
     if (expand) L.pos = a.exp_pos[i];
     L.e = (e >= 0 && e < a.E) ? static_cast<int>(e) : -1;
   }
-  const bool valid = L.e >= 0 && (expand ? L.pos >= 0 : L.slot >= 0);
+  const bool valid = L.e >= 0 && (atomic || (expand ? L.pos >= 0 : L.slot >= 0));
   L.d = valid ? L.e / a.L : -1 - lane;
   const unsigned same = __match_any_sync(kFullMask, L.d);
   L.vmask = __ballot_sync(kFullMask, valid);
   L.rmask = __ballot_sync(kFullMask, valid && (same & lanemask_lt()) == 0);
+  if (atomic) {
+    const int s = static_cast<int>(tok / a.T);
+    const int rb = a.n_so == 1 ? s : (s % a.n_su) * a.n_so + s / a.n_su;
+    int mine = -1;
+    if ((L.rmask >> lane) & 1) mine = rb * a.M + atomicAdd(a.send_counters + s * a.R + L.d, 1);
+    L.slot = __shfl_sync(kFullMask, mine, __ffs(same) - 1);
+    if (!valid) L.slot = -1;
+  }
   L.row = (valid && !expand) ? recv_row_of_slot(L.slot, L.d, a.R, a.M, a.compact, a.recv_psum) : -1;
   return L;
 }
 
-template <int kKind, bool kExpand>
+template <int kKind, bool kExpand, bool kAtomic = false>
 __global__ void __launch_bounds__(kCopyThreads) dispatch_kernel(DispatchArgs a) {
   __shared__ int64_t s_row[kWarps][kMaxTopk];               // hidden destination rows
   __shared__ float s_sf[kWarps][kMaxScaleGroups];           // this token's FP8 scales
@@ -66,7 +78,7 @@ __global__ void __launch_bounds__(kCopyThreads) dispatch_kernel(DispatchArgs a) 
   for (int64_t tok = gwarp; tok < a.num_tokens; tok += nwarps) {
     const int s = static_cast<int>(tok / a.T);
     const int t = static_cast<int>(tok - static_cast<int64_t>(s) * a.T);
-    const TokenLanes ln = load_lanes(a, tok, lane, kExpand);
+    const TokenLanes ln = load_lanes(a, tok, lane, kExpand, kAtomic);
     const unsigned hmask = kExpand ? ln.vmask : ln.rmask;
     if ((hmask >> lane) & 1) {
       const int64_t row = kExpand ? static_cast<int64_t>(a.exp_region[ln.d]) + ln.pos
@@ -195,17 +207,36 @@ __global__ void __launch_bounds__(kCopyThreads) dispatch_kernel(DispatchArgs a) 
     }
     __syncwarp();  // s_row / s_sf are rewritten by the next token
   }
+
+  // expanded blocks padded to expert_alignment: zero the rows after each
+  // expert's lanes up to the next block start (and their scales)
+  if (kExpand && a.zero_padding) {
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    const int nchunk = a.out_row_bytes >> 4;
+    for (int64_t blk = gwarp; blk < a.E; blk += nwarps) {
+      const int d = static_cast<int>(blk / a.L), j = static_cast<int>(blk % a.L);
+      const int64_t region = a.exp_region[d];
+      const int64_t first = region + a.exp_base[d * (a.L + 1) + j] + a.exp_cnt[blk];
+      const int64_t end = region + a.exp_base[d * (a.L + 1) + j + 1];
+      for (int64_t row = first; row < end; ++row) {
+        uint8_t* dst = a.recv_x + row * a.out_row_bytes;
+        for (int c = lane; c < nchunk; c += 32) st16(dst + (static_cast<size_t>(c) << 4), zero);
+        if (kKind == kCastRow || a.x_sf != nullptr)
+          for (int g = lane; g < a.G; g += 32) a.recv_sf[row * a.G + g] = 0.f;
+      }
+    }
+  }
 }
 
-template <int kKind, bool kExpand>
+template <int kKind, bool kExpand, bool kAtomic = false>
 cudaError_t launch_one(const DispatchArgs& a, int num_sms, cudaStream_t stream) {
-  auto kern = dispatch_kernel<kKind, kExpand>;
+  auto kern = dispatch_kernel<kKind, kExpand, kAtomic>;
   int per_sm = 0;
   cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kCopyThreads, 0);
   if (err != cudaSuccess) return err;
   if (per_sm < 1) per_sm = 1;
   int64_t ctas = static_cast<int64_t>(num_sms) * per_sm;
-  const int64_t need = (a.num_tokens + kWarps - 1) / kWarps;
+  const int64_t need = ((a.zero_padding && a.E > a.num_tokens ? a.E : a.num_tokens) + kWarps - 1) / kWarps;
   if (ctas > need) ctas = need;
   if (ctas < 1) return cudaSuccess;
   kern<<<static_cast<unsigned>(ctas), kCopyThreads, 0, stream>>>(a);
@@ -223,6 +254,13 @@ cudaError_t launch_dispatch(const Geometry& g, const DispatchArgs& a, int num_sm
   }
   return g.expand ? launch_one<kCopyRow, true>(a, num_sms, stream)
                   : launch_one<kCopyRow, false>(a, num_sms, stream);
+}
+
+cudaError_t launch_dispatch_atomic(const Geometry& g, const DispatchArgs& a, int num_sms,
+                                   cudaStream_t stream) {
+  const bool cast = !g.x_fp8 && g.recv_fp8;
+  return cast ? launch_one<kCastRow, false, true>(a, num_sms, stream)
+              : launch_one<kCopyRow, false, true>(a, num_sms, stream);
 }
 
 }  // namespace ep

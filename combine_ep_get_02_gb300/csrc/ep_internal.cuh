@@ -16,6 +16,7 @@ constexpr int kMaxExperts = 4096;
 constexpr int kMaxScaleGroups = 128;  // FP8 receive: hidden <= 128 * 128
 constexpr int kCopyThreads = 256;     // dispatch / combine CTA size (8 warps)
 constexpr int kMaxPrologueCtas = 64;
+constexpr int kMaxSortRows = 8192;   // rows of one segment the comparison sort handles
 
 // device error bits latched in the workspace header
 constexpr uint32_t kErrBadTopk = 1u;
@@ -24,7 +25,7 @@ constexpr uint32_t kErrOverflow = 2u;
 // Sizes derived from an ep_config_t that passed validation.
 struct Geometry {
   int R, n_so, n_su, E, L, K, T, M, H, G;
-  int x_fp8, recv_fp8, expand, align, compact;
+  int x_fp8, recv_fp8, expand, align, compact, zero_padding;
   int64_t region_rows;  // rows of one destination region in the row form: R * M
   int64_t num_tokens;   // R * T
 };
@@ -71,15 +72,37 @@ struct DispatchArgs {
   const int32_t* exp_pos;
   const int32_t* exp_region;
   const int32_t* recv_psum;  // compact receive rows only
+  const int32_t* exp_cnt;    // zero padding only
+  const int32_t* exp_base;   // zero padding only
+  int32_t* send_counters;    // atomic-slot comparison path only: [R src][R dst]
   uint8_t* recv_x;
   float* recv_sf;
   int64_t* recv_idx;
   float* recv_w;
   int32_t* recv_md;
-  int R, E, L, K, T, H, G, M, compact;
+  int R, E, L, K, T, H, G, M, compact, zero_padding, n_so, n_su;
   int64_t region_rows;
   int64_t num_tokens;
   int in_row_bytes, out_row_bytes;
+};
+
+// The post-hoc sort of the comparison path: permutes each (destination, row
+// block) segment of a receive buffer into source-token order.
+struct SortArgs {
+  const uint8_t* in_x;
+  const float* in_sf;
+  const int64_t* in_idx;
+  const float* in_w;
+  const int32_t* in_md;
+  uint8_t* out_x;
+  float* out_sf;
+  int64_t* out_idx;
+  float* out_w;
+  int32_t* out_md;
+  const int32_t* send_counters;  // [R src][R dst]: rows each source sent each destination
+  int R, K, M, G, n_so, n_su;
+  int64_t region_rows;
+  int row_bytes;
 };
 
 struct CombineArgs {
@@ -100,6 +123,9 @@ cudaError_t launch_layout(const Geometry& g, const LayoutArgs& a, int num_prolog
                           cudaStream_t stream);
 cudaError_t launch_dispatch(const Geometry& g, const DispatchArgs& a, int num_sms,
                             cudaStream_t stream);
+cudaError_t launch_dispatch_atomic(const Geometry& g, const DispatchArgs& a, int num_sms,
+                                   cudaStream_t stream);
+cudaError_t launch_sort(const Geometry& g, const SortArgs& a, cudaStream_t stream);
 cudaError_t launch_combine(const Geometry& g, const CombineArgs& a, int num_sms,
                            cudaStream_t stream);
 

@@ -82,6 +82,10 @@ typedef struct ep_config {
                                       row-block order ([P690] Direct Recv X: the entries
                                       of row block i start at the exclusive prefix
                                       recv_psum[d][i-1] of the receive counts)    */
+  int32_t zero_padding;            /* expanded only: 1 = dispatch writes zeros into the
+                                      rows between each expert's lanes and the next
+                                      expert_alignment boundary (and their FP8
+                                      scales); 0 = those rows are left untouched  */
 } ep_config_t;
 
 /* ---- dispatch layout (all device pointers, int32 unless noted) -------------
@@ -203,6 +207,31 @@ int ep_dispatch(const ep_config_t* cfg, const ep_layout_t* layout, const void* x
 int ep_combine(const ep_config_t* cfg, const ep_layout_t* layout, const uint16_t* y,
                const int64_t* topk_idx, const float* topk_weights, uint16_t* out,
                void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---- comparison path: the design PR #753 replaces ----------------------------
+ * [P753 Motivation] Before kernel-side slots, a sender took its destination slot
+ * with an atomicAdd on a shared counter, so the order of a source's rows inside
+ * a destination depended on the race between warps, and EPHandle.deterministic_sort
+ * restored a reproducible order afterwards by sorting the received tokens by
+ * source token and permuting every order-dependent tensor. These two entry points
+ * reproduce that path (row form only, not compact) so it can be measured against
+ * ep_get_dispatch_layout + ep_dispatch; after the sort the buffers equal the
+ * deterministic dispatch's bit for bit.
+ *
+ * ep_dispatch_atomic: ep_dispatch without a layout. send_counters: device int32
+ * [R src][R dst], zeroed on `stream` by the call, then left holding how many
+ * rows each source sent each destination. Rows land in the source's row block
+ * of the destination region in race order. */
+int ep_dispatch_atomic(const ep_config_t* cfg, const void* x, const float* x_sf,
+                       const int64_t* topk_idx, const float* topk_weights, const ep_recv_t* recv,
+                       int32_t* send_counters, void* stream);
+
+/* ep_deterministic_sort: sorts every (destination, row block) segment of `recv`
+ * (filled by ep_dispatch_atomic; the sidecars must be present: the key is the
+ * metadata's source token) and writes rows and sidecars in that order to
+ * `sorted` (same shapes). num_max_tokens_per_rank <= 8192. */
+int ep_deterministic_sort(const ep_config_t* cfg, const ep_recv_t* recv,
+                          const int32_t* send_counters, const ep_recv_t* sorted, void* stream);
 
 /* Synchronises `stream`, returns the first device-detected error latched in
  * the workspace since the last call (EP_OK if none) and clears it. */

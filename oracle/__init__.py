@@ -26,7 +26,7 @@ OK, INVALID, UNSUPPORTED, BAD_TOPK, OVERFLOW = 0, -1, -2, -5, -6
 class _Cfg(C.Structure):
     _fields_ = [(n, C.c_int32) for n in
                 ("n_so", "n_su", "E", "K", "T", "M", "H", "x_fp8", "recv_fp8", "expand", "align",
-                 "compact")]
+                 "compact", "zero_padding")]
 
 
 _lib = None
@@ -58,7 +58,7 @@ def lib():
         L.orc_dispatch_token.restype = C.c_int
         L.orc_dispatch_token.argtypes = [P, C.c_int, C.c_int] + [P] * 16
         L.orc_dispatch.restype = C.c_int
-        L.orc_dispatch.argtypes = [P] * 14
+        L.orc_dispatch.argtypes = [P] * 16
         L.orc_combine_token.restype = None
         L.orc_combine_token.argtypes = [C.c_int, C.c_int, P, P, P]
         L.orc_combine_gathered.restype = None
@@ -77,7 +77,8 @@ def cfg_of(wl) -> _Cfg:
     return _Cfg(wl.n_so, wl.n_su, wl.num_experts, wl.num_topk, wl.num_tokens,
                 wl.num_max_tokens_per_rank, wl.hidden, int(wl.x_dtype == "fp8"),
                 int(wl.recv_dtype == "fp8"), int(bool(wl.expand)), wl.expert_alignment,
-                int(bool(getattr(wl, "compact", False))))
+                int(bool(getattr(wl, "compact", False))),
+                int(bool(getattr(wl, "zero_padding", False))))
 
 
 def _np(a, dtype):
@@ -216,11 +217,11 @@ def dispatch_token(wl, lay, s, t, x_row, x_sf_row, idx_tok, w_tok):
                 meta_idx=meta_idx[:n_meta], meta_w=meta_w[:n_meta], meta_md=meta_md[:n_meta])
 
 
-def dispatch(wl, lay, x, x_sf, topk_idx, topk_weights):
+def dispatch(wl, lay, x, x_sf, topk_idx, topk_weights, fill=0):
     """Full dispatch. Returns (status, dict): recv_x [rows, H] (uint16 bf16 bits or
     uint8 e4m3 codes), recv_sf [rows, G] or None, recv_topk_idx [R, R*M, K],
     recv_topk_weights [R, R*M, K], recv_src_metadata [R, R*M, 2+K]. Rows that no
-    entry fills stay zero."""
+    entry fills keep the byte value `fill`."""
     c = cfg_of(wl)
     R, K, H, M = wl.num_ranks, wl.num_topk, wl.hidden, wl.num_max_tokens_per_rank
     G = H // 128
@@ -230,15 +231,15 @@ def dispatch(wl, lay, x, x_sf, topk_idx, topk_weights):
     xa = _np(x, np.uint8 if fp8_in else np.uint16)
     sfa = None if x_sf is None else _np(x_sf, np.float32)
     out = dict(
-        recv_x=np.zeros((rows, H), np.uint8 if fp8_out else np.uint16),
-        recv_sf=np.zeros((rows, G), np.float32) if fp8_out else None,
+        recv_x=np.full((rows, H * (1 if fp8_out else 2)), fill, np.uint8).view(np.uint8 if fp8_out else np.uint16),
+        recv_sf=np.full((rows, G * 4), fill, np.uint8).view(np.float32) if fp8_out else None,
         recv_topk_idx=np.zeros((R, R * M, K), np.int64),
         recv_topk_weights=np.zeros((R, R * M, K), np.float32),
         recv_src_metadata=np.zeros((R, R * M, 2 + K), np.int32),
     )
     st = lib().orc_dispatch(
         C.byref(c), _p(lay["slot_map"]), _p(lay.get("exp_pos")), _p(lay.get("exp_region")),
-        _p(lay["recv_psum"]), _p(xa), _p(sfa), _p(_np(topk_idx, np.int64)), _p(_np(topk_weights, np.float32)),
+        _p(lay.get("exp_cnt")), _p(lay.get("exp_base")), _p(lay["recv_psum"]), _p(xa), _p(sfa), _p(_np(topk_idx, np.int64)), _p(_np(topk_weights, np.float32)),
         _p(out["recv_x"]), _p(out["recv_sf"]), _p(out["recv_topk_idx"]),
         _p(out["recv_topk_weights"]), _p(out["recv_src_metadata"]))
     return st, out

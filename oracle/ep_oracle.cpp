@@ -52,7 +52,7 @@ namespace {
 
 struct Cfg {
   int32_t n_so, n_su, E, K, T, M, H;
-  int32_t x_fp8, recv_fp8, expand, align, compact;
+  int32_t x_fp8, recv_fp8, expand, align, compact, zero_padding;
 };
 
 constexpr int kOk = 0;
@@ -153,6 +153,7 @@ int check_cfg(const Cfg& c) {
   if ((c.x_fp8 || c.recv_fp8) && c.H % 128 != 0) return kInvalid;
   if (c.x_fp8 && !c.recv_fp8) return kUnsupported;
   if (c.compact && c.expand) return kUnsupported;
+  if (c.zero_padding && !c.expand) return kUnsupported;
   return kOk;
 }
 
@@ -196,7 +197,7 @@ extern "C" {
 
 struct orc_cfg {
   int32_t n_so, n_su, E, K, T, M, H;
-  int32_t x_fp8, recv_fp8, expand, align, compact;
+  int32_t x_fp8, recv_fp8, expand, align, compact, zero_padding;
 };
 
 static Cfg to_cfg(const orc_cfg* p) {
@@ -427,7 +428,8 @@ int orc_dispatch_token(const orc_cfg* p, int s, int t, const int32_t* slot_tok,
 // In the row form, destination d's rows start at d*R*M; expanded rows at
 // exp_region[d].
 int orc_dispatch(const orc_cfg* p, const int32_t* slot_map, const int32_t* exp_pos,
-                 const int32_t* exp_region, const int32_t* recv_psum, const void* x, const float* x_sf,
+                 const int32_t* exp_region, const int32_t* exp_cnt, const int32_t* exp_base,
+                 const int32_t* recv_psum, const void* x, const float* x_sf,
                  const int64_t* topk_idx, const float* topk_weights, void* recv_x,
                  float* recv_sf, int64_t* recv_topk_idx, float* recv_topk_weights,
                  int32_t* recv_src_metadata) {
@@ -467,6 +469,22 @@ int orc_dispatch(const orc_cfg* p, const int32_t* slot_map, const int32_t* exp_p
         if (recv_topk_weights) std::memcpy(recv_topk_weights + row * K, &meta_w[i * K], 4 * K);
         if (recv_src_metadata)
           std::memcpy(recv_src_metadata + row * (2 + K), &meta_md[i * (2 + K)], 4 * (2 + K));
+      }
+    }
+  }
+  // expanded blocks padded to expert_alignment: with zero padding, the rows
+  // after each expert's lanes up to the next block start are zero (and so are
+  // their FP8 scales)
+  if (c.expand && c.zero_padding) {
+    const int L = c.E / R;
+    for (int d = 0; d < R; ++d) {
+      for (int j = 0; j < L; ++j) {
+        const int64_t first = static_cast<int64_t>(exp_region[d]) + exp_base[d * (L + 1) + j] + exp_cnt[d * L + j];
+        const int64_t end = static_cast<int64_t>(exp_region[d]) + exp_base[d * (L + 1) + j + 1];
+        for (int64_t row = first; row < end; ++row) {
+          std::memset(static_cast<uint8_t*>(recv_x) + row * H * out_eb, 0, H * out_eb);
+          if (c.recv_fp8) std::memset(recv_sf + row * G, 0, sizeof(float) * G);
+        }
       }
     }
   }

@@ -82,6 +82,8 @@ def test_workspace_bytes_closed_form(ep):
     (dict(x_dtype=7), -1),
     (dict(compact_recv=2), -1),
     (dict(compact_recv=1, expand=1), -2),     # expanded rows are packed already
+    (dict(zero_padding=1), -2),               # only expanded blocks have padding
+    (dict(zero_padding=3, expand=1), -1),
 ])
 def test_invalid_configs_are_rejected_before_any_launch(ep, bad, code):
     c = cfg(ep, **bad)

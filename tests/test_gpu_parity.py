@@ -237,3 +237,67 @@ def test_device_conversions_match_oracle_on_every_float(kind):
             got = got.view(exp.dtype)
             for sl in _non_nan_slices(first, chunk):
                 assert np.array_equal(got[sl], exp[sl]), (hex(first), sl)
+
+
+@pytest.mark.parametrize("name,x_dtype,recv", [("expanded_a128_zero", "bf16", "bf16"),
+                                               ("expanded_a128_zero", "bf16", "fp8"),
+                                               ("expanded_a128_zero", "fp8", "fp8")])
+def test_zero_padding_rows(name, x_dtype, recv):
+    """Expanded blocks aligned to 128 rows: with zero padding every row of every
+    region is either a lane's row or zero (PR #753 Compatibility: kDoZeroPadding,
+    kExpertAlignment); checked over the whole used buffer, prefilled with 0xFF."""
+    wl = W.PARITY[name].replace(x_dtype=x_dtype, recv_dtype=recv, hidden=512)
+    idx, w, x, sf = inputs(wl)
+    st, olay = oracle.layout(wl, idx)
+    run = GpuRun(wl, idx, w, x, sf).layout()
+    run.recv = ep.alloc_recv(run.cfg, run.dev)
+    run.recv.recv_x.view(torch.uint8).fill_(0xFF)
+    if run.recv.recv_sf is not None:
+        run.recv.recv_sf.view(torch.uint8).fill_(0xFF)
+    run.dispatch()
+    assert run.status() == ep.EP_OK
+    st, orec = oracle.dispatch(wl, olay, x, sf, idx, w, fill=0xFF)
+    used = int(olay["exp_region"][-1])
+    assert used % 128 == 0 and used > int(olay["exp_cnt"].sum())
+    got = run.recv.recv_x[:used].contiguous().view(torch.uint8).cpu().numpy()
+    assert np.array_equal(got, orec["recv_x"][:used].view(np.uint8))
+    if recv == "fp8":
+        assert np.array_equal(run.recv.recv_sf[:used].cpu().numpy().view(np.uint32),
+                              orec["recv_sf"][:used].view(np.uint32))
+
+
+def test_cached_redispatch_replays_the_stored_layout():
+    """Cached mode: a second dispatch with new activations reuses the stored
+    layout (no prologue) and lands every row where the oracle puts it."""
+    wl = W.PARITY["dsv3_fp8"]
+    idx, w, x, sf = inputs(wl)
+    st, olay = oracle.layout(wl, idx)
+    run = GpuRun(wl, idx, w, x, sf).layout().dispatch()
+    x2 = torch.randn(x.shape, generator=torch.Generator().manual_seed(77)).to(torch.bfloat16)
+    run.x = x2.to(run.dev)
+    run.dispatch()  # layout not recomputed
+    assert run.status() == ep.EP_OK
+    st, orec = oracle.dispatch(wl, olay, x2, sf, idx, w)
+    compare_dispatch(run, olay, orec)
+
+
+@pytest.mark.parametrize("name", ["direct_zipf", "hybrid_rowform", "dsv3_fp8", "dsv3_fp8_precast"])
+def test_atomic_slots_plus_sort_equal_the_deterministic_dispatch(name):
+    """PR #753 Motivation/Approach: racing atomicAdd slots followed by the
+    post-hoc sort by source token give exactly the kernel-side deterministic
+    placement (every receive tensor, bit for bit)."""
+    wl = W.PARITY[name]
+    idx, w, x, sf = inputs(wl)
+    det = GpuRun(wl, idx, w, x, sf).layout().dispatch()
+    racy = ep.alloc_recv(det.cfg, det.dev, zero=True)
+    counters = torch.full((wl.num_ranks, wl.num_ranks), 7, dtype=torch.int32, device=det.dev)
+    ep.ep_dispatch_atomic(det.cfg, det.x, det.sf, det.idx, det.w, racy, counters)
+    assert torch.equal(counters, det.lay.num_tokens_per_rank)
+    srt = ep.alloc_recv(det.cfg, det.dev, zero=True)
+    ep.ep_deterministic_sort(det.cfg, racy, counters, srt)
+    torch.cuda.synchronize()
+    for f in ("recv_x", "recv_sf", "recv_topk_idx", "recv_topk_weights", "recv_src_metadata"):
+        a, b = getattr(det.recv, f), getattr(srt, f)
+        if a is None:
+            continue
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), f

@@ -280,3 +280,26 @@ def test_compact_and_row_form_give_the_same_combine(orc, name):
                 n = int(lay["recv_cnt"][d].sum())
                 assert np.all(md[d, :n, 0] >= 0) and not md[d, n:].any()
     assert np.array_equal(outs[0], outs[1])
+
+
+def test_zero_padding_of_aligned_expanded_blocks(orc):
+    """Expanded blocks padded to the alignment: rows between an expert's lanes
+    and the next block start are zero with zero padding, untouched without."""
+    wl = W.PARITY["expanded_a128_zero"].replace(num_tokens=20, num_max_tokens_per_rank=20, hidden=128,
+                                                expert_alignment=8)
+    idx, w = W.routing(wl)
+    x, _ = W.hidden(wl)
+    _, lay = orc.layout(wl, idx)
+    R, L = wl.num_ranks, wl.num_experts // wl.num_ranks
+    pad = []
+    for d in range(R):
+        for j in range(L):
+            a = lay["exp_region"][d] + lay["exp_base"][d, j] + lay["exp_cnt"][d, j]
+            b = lay["exp_region"][d] + lay["exp_base"][d, j + 1]
+            assert b - a < wl.expert_alignment and (b - lay["exp_region"][d]) % wl.expert_alignment == 0
+            pad.extend(range(a, b))
+    assert pad
+    st, rec = orc.dispatch(wl, lay, x, None, idx, w, fill=0xFF)
+    assert st == 0 and not rec["recv_x"][pad].any()
+    st, rec = orc.dispatch(wl.replace(zero_padding=False), lay, x, None, idx, w, fill=0xFF)
+    assert np.all(rec["recv_x"][pad] == 0xFFFF)

@@ -47,6 +47,7 @@ class Workload:
     expand: bool = False
     expert_alignment: int = 1
     compact: bool = False         # compact receive rows (row form only)
+    zero_padding: bool = False    # zero the alignment padding rows (expanded only)
     routing: str = "gauss"        # "gauss" | "zipf" | "hot"
     zipf_s: float = 1.1
     mask_frac: float = 0.0
@@ -101,6 +102,10 @@ PARITY = {
         name="direct_zipf_compact", compact=True, num_tokens=300, num_max_tokens_per_rank=320),
     "hybrid_compact": WORKLOADS["hybrid_rowform"].replace(
         name="hybrid_compact", compact=True, num_tokens=300, num_max_tokens_per_rank=300),
+    # expanded blocks aligned to 128 rows with zeroed padding
+    "expanded_a128_zero": WORKLOADS["expanded"].replace(
+        name="expanded_a128_zero", expert_alignment=128, zero_padding=True, num_tokens=100,
+        num_max_tokens_per_rank=100),
 }
 
 
