@@ -48,6 +48,8 @@ def parse():
                    help="compact receive rows (each destination packed from row 0)")
     p.add_argument("--align", type=int, default=0, help="expert_alignment of the expanded layout")
     p.add_argument("--zero-padding", action="store_true", help="zero the alignment padding rows")
+    p.add_argument("--sf-pack", action="store_true",
+                   help="packed power-of-two FP8 scales (4 exponent bytes per word)")
     p.add_argument("--cached", action="store_true",
                    help="time dispatch + combine only, replaying a layout computed once")
     p.add_argument("--compare-sort", action="store_true",
@@ -68,6 +70,8 @@ def workload(args):
         wl = wl.replace(expert_alignment=args.align)
     if args.zero_padding:
         wl = wl.replace(zero_padding=True)
+    if args.sf_pack:
+        wl = wl.replace(sf_pack=True)
     return wl
 
 
@@ -78,7 +82,8 @@ def describe(wl) -> str:
         lay += ", compact receive rows"
     if wl.expand and wl.expert_alignment > 1:
         lay += f", blocks aligned to {wl.expert_alignment}" + (" with zeroed padding" if wl.zero_padding else "")
-    cast = {("bf16", "fp8"): "bf16 x cast to fp8-e4m3 inside dispatch (fp32 scale per 128 columns)",
+    cast = {("bf16", "fp8"): "bf16 x cast to fp8-e4m3 inside dispatch (" + (
+                "packed power-of-two scale per 128 columns" if wl.sf_pack else "fp32 scale per 128 columns") + ")",
             ("fp8", "fp8"): "pre-cast fp8-e4m3 x + fp32 scales",
             ("bf16", "bf16"): "bf16 rows"}[(wl.x_dtype, wl.recv_dtype)]
     return (f"{wl.name}: {wl.num_ranks} logical ranks x {wl.num_tokens} tokens, {wl.num_experts} experts "
@@ -109,11 +114,12 @@ def algorithmic_bytes(wl, ntpr, valid_lanes, tokens_with_lane, pad_rows=0):
     layout = n_tok * K * 8 + n_tok * K * 4 + n_tok * R + 4 * R * (R + wl.num_experts) * 2
     if wl.expand:
         layout += n_tok * K * 4
+    SW = ((G + 3) // 4 if wl.sf_pack else G) * 4                  # scale bytes per row
     dispatch = (tokens_with_lane * H * eb_in                       # x read once per routed token
-                + (tokens_with_lane * G * 4 if wl.x_dtype == "fp8" else 0)
+                + (tokens_with_lane * SW if wl.x_dtype == "fp8" else 0)
                 + hid_rows * H * eb_out                            # hidden rows written
-                + (hid_rows * G * 4 if wl.recv_dtype == "fp8" else 0)
-                + pad_rows * (H * eb_out + (G * 4 if wl.recv_dtype == "fp8" else 0))  # zeroed padding
+                + (hid_rows * SW if wl.recv_dtype == "fp8" else 0)
+                + pad_rows * (H * eb_out + (SW if wl.recv_dtype == "fp8" else 0))  # zeroed padding
                 + ntpr * (K * 8 + K * 4 + (2 + K) * 4)             # sidecar rows
                 + n_tok * K * (8 + 4 + 4))                         # topk_idx, weights, slots read
     combine = (hid_rows * H * 2                                    # each expert-output row once

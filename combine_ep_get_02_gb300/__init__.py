@@ -43,7 +43,7 @@ class _Config(C.Structure):
     _fields_ = [(n, C.c_int32) for n in (
         "num_scaleout_ranks", "num_scaleup_ranks", "num_experts", "num_topk", "num_tokens",
         "num_max_tokens_per_rank", "hidden", "x_dtype", "recv_dtype", "expand", "expert_alignment",
-        "num_sms", "num_prologue_sms", "compact_recv", "zero_padding")]
+        "num_sms", "num_prologue_sms", "compact_recv", "zero_padding", "sf_pack")]
 
 
 class _Layout(C.Structure):
@@ -75,6 +75,7 @@ class Config:
     num_prologue_sms: int = 0
     compact_recv: int = 0
     zero_padding: int = 0
+    sf_pack: int = 0
 
     @property
     def num_ranks(self) -> int:
@@ -92,7 +93,8 @@ def config_of(wl, **over) -> Config:
                EP_DTYPE_FP8_E4M3 if wl.recv_dtype == "fp8" else EP_DTYPE_BF16,
                int(bool(wl.expand)), wl.expert_alignment,
                compact_recv=int(bool(getattr(wl, "compact", False))),
-               zero_padding=int(bool(getattr(wl, "zero_padding", False))))
+               zero_padding=int(bool(getattr(wl, "zero_padding", False))),
+               sf_pack=int(bool(getattr(wl, "sf_pack", False))))
     return dataclasses.replace(c, **over)
 
 
@@ -233,7 +235,8 @@ def alloc_recv(cfg: Config, device="cuda", sidecars: bool = True, zero: bool = F
     mk = torch.zeros if zero else torch.empty
     fp8 = cfg.recv_dtype == EP_DTYPE_FP8_E4M3
     recv_x = mk(rows, H, dtype=torch.uint8 if fp8 else torch.bfloat16, device=device)
-    recv_sf = mk(rows, H // 128, dtype=torch.float32, device=device) if fp8 else None
+    G = H // 128
+    recv_sf = mk(rows, (G + 3) // 4 if cfg.sf_pack else G, dtype=torch.float32, device=device) if fp8 else None
     if not sidecars:
         return Recv(recv_x, recv_sf, None, None, None)
     return Recv(recv_x, recv_sf, mk(R, R * M, K, dtype=torch.int64, device=device),

@@ -76,6 +76,8 @@ int make_geometry(const ep_config_t* c, Geometry* g) {
   if (c->compact_recv && c->expand) return EP_ERR_UNSUPPORTED;  // expanded rows are packed already
   if (c->zero_padding != 0 && c->zero_padding != 1) return EP_ERR_INVALID_ARG;
   if (c->zero_padding && !c->expand) return EP_ERR_UNSUPPORTED;  // only expanded blocks are padded
+  if (c->sf_pack != 0 && c->sf_pack != 1) return EP_ERR_INVALID_ARG;
+  if (c->sf_pack && c->recv_dtype != EP_DTYPE_FP8_E4M3) return EP_ERR_UNSUPPORTED;
   // 32-bit row indices: rows of one region, lanes, and expanded rows must fit
   const int64_t region_rows = R * c->num_max_tokens_per_rank;
   const int64_t lanes = R * c->num_tokens * c->num_topk;
@@ -98,6 +100,8 @@ int make_geometry(const ep_config_t* c, Geometry* g) {
   g->align = c->expert_alignment;
   g->compact = c->compact_recv;
   g->zero_padding = c->zero_padding;
+  g->sf_pack = c->sf_pack;
+  g->SW = c->sf_pack ? (g->G + 3) / 4 : g->G;
   g->region_rows = region_rows;
   g->num_tokens = R * c->num_tokens;
   return EP_OK;
@@ -263,6 +267,8 @@ int ep_dispatch(const ep_config_t* cfg, const ep_layout_t* layout, const void* x
   a.M = g.M;
   a.compact = g.compact;
   a.zero_padding = g.zero_padding;
+  a.sf_pack = g.sf_pack;
+  a.SW = g.SW;
   a.region_rows = g.region_rows;
   a.num_tokens = g.num_tokens;
   a.in_row_bytes = g.H * (g.x_fp8 ? 1 : 2);
@@ -352,6 +358,8 @@ int ep_dispatch_atomic(const ep_config_t* cfg, const void* x, const float* x_sf,
   a.M = g.M;
   a.n_so = g.n_so;
   a.n_su = g.n_su;
+  a.sf_pack = g.sf_pack;
+  a.SW = g.SW;
   a.region_rows = g.region_rows;
   a.num_tokens = g.num_tokens;
   a.in_row_bytes = g.H * (g.x_fp8 ? 1 : 2);
@@ -392,7 +400,7 @@ int ep_deterministic_sort(const ep_config_t* cfg, const ep_recv_t* recv,
   a.R = g.R;
   a.K = g.K;
   a.M = g.M;
-  a.G = g.G;
+  a.SW = g.SW;
   a.n_so = g.n_so;
   a.n_su = g.n_su;
   a.region_rows = g.region_rows;

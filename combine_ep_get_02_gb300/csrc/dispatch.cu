@@ -108,11 +108,11 @@ __global__ void __launch_bounds__(kCopyThreads) dispatch_kernel(DispatchArgs a) 
           }
         }
       }
-      if (a.x_sf != nullptr) {  // pre-cast FP8: the scales travel verbatim
-        const float* ssrc = a.x_sf + tok * a.G;
-        for (int g = lane; g < a.G; g += 32) {
+      if (a.x_sf != nullptr) {  // pre-cast FP8: the scale words travel verbatim
+        const float* ssrc = a.x_sf + tok * a.SW;
+        for (int g = lane; g < a.SW; g += 32) {
           const float v = ssrc[g];
-          for (int j = 0; j < nh; ++j) a.recv_sf[s_row[warp][j] * a.G + g] = v;
+          for (int j = 0; j < nh; ++j) a.recv_sf[s_row[warp][j] * a.SW + g] = v;
         }
       }
     } else {
@@ -148,7 +148,12 @@ __global__ void __launch_bounds__(kCopyThreads) dispatch_kernel(DispatchArgs a) 
           amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 2));
           amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 4));
           amax = fmaxf(amax, 1e-4f);
-          const float inv = __fdiv_rn(448.0f, amax);
+          // fp32 scale: inv = 448/amax. Packed: the smallest 2^e >= amax/448, read off
+          // amax's exponent and mantissa (amax = m*2^k; e = k-8, or k-7 when m > 1.75).
+          const uint32_t ab = __float_as_uint(amax);
+          const int e2 = static_cast<int>(ab >> 23) - 127 - 8 + ((ab & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+          const float inv = a.sf_pack ? __uint_as_float(static_cast<uint32_t>(127 - e2) << 23)
+                                      : __fdiv_rn(448.0f, amax);
           uint4 q;
           q.x = f32x2_to_e4m3x2(__fmul_rn(f[0], inv), __fmul_rn(f[1], inv)) |
                 f32x2_to_e4m3x2(__fmul_rn(f[2], inv), __fmul_rn(f[3], inv)) << 16;
@@ -159,16 +164,31 @@ __global__ void __launch_bounds__(kCopyThreads) dispatch_kernel(DispatchArgs a) 
           q.w = f32x2_to_e4m3x2(__fmul_rn(f[12], inv), __fmul_rn(f[13], inv)) |
                 f32x2_to_e4m3x2(__fmul_rn(f[14], inv), __fmul_rn(f[15], inv)) << 16;
           if (u < nunit) {
-            if ((lane & 7) == 0) s_sf[warp][u >> 3] = __fdiv_rn(amax, 448.0f);
+            if ((lane & 7) == 0) {
+              if (a.sf_pack) reinterpret_cast<uint8_t*>(s_sf[warp])[u >> 3] = static_cast<uint8_t>(e2 + 127);
+              else s_sf[warp][u >> 3] = __fdiv_rn(amax, 448.0f);
+            }
             for (int j = 0; j < nh; ++j)
               st16(a.recv_x + s_row[warp][j] * a.out_row_bytes + (static_cast<size_t>(u) << 4), q);
           }
         }
       }
       __syncwarp();
-      for (int g = lane; g < a.G; g += 32) {
-        const float v = s_sf[warp][g];
-        for (int j = 0; j < nh; ++j) a.recv_sf[s_row[warp][j] * a.G + g] = v;
+      if (a.sf_pack) {  // four exponent bytes per word; bytes past the last group are 0
+        const uint8_t* b = reinterpret_cast<const uint8_t*>(s_sf[warp]);
+        for (int wd = lane; wd < a.SW; wd += 32) {
+          uint32_t v = 0;
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (4 * wd + i < a.G) v |= static_cast<uint32_t>(b[4 * wd + i]) << (8 * i);
+          for (int j = 0; j < nh; ++j)
+            reinterpret_cast<uint32_t*>(a.recv_sf)[s_row[warp][j] * a.SW + wd] = v;
+        }
+      } else {
+        for (int g = lane; g < a.G; g += 32) {
+          const float v = s_sf[warp][g];
+          for (int j = 0; j < nh; ++j) a.recv_sf[s_row[warp][j] * a.G + g] = v;
+        }
       }
     }
 
@@ -222,7 +242,7 @@ __global__ void __launch_bounds__(kCopyThreads) dispatch_kernel(DispatchArgs a) 
         uint8_t* dst = a.recv_x + row * a.out_row_bytes;
         for (int c = lane; c < nchunk; c += 32) st16(dst + (static_cast<size_t>(c) << 4), zero);
         if (kKind == kCastRow || a.x_sf != nullptr)
-          for (int g = lane; g < a.G; g += 32) a.recv_sf[row * a.G + g] = 0.f;
+          for (int g = lane; g < a.SW; g += 32) a.recv_sf[row * a.SW + g] = 0.f;
       }
     }
   }

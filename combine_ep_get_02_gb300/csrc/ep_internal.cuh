@@ -25,7 +25,8 @@ constexpr uint32_t kErrOverflow = 2u;
 // Sizes derived from an ep_config_t that passed validation.
 struct Geometry {
   int R, n_so, n_su, E, L, K, T, M, H, G;
-  int x_fp8, recv_fp8, expand, align, compact, zero_padding;
+  int x_fp8, recv_fp8, expand, align, compact, zero_padding, sf_pack;
+  int SW;  // 32-bit words of one row's scale sidecar: G, or ceil(G/4) packed
   int64_t region_rows;  // rows of one destination region in the row form: R * M
   int64_t num_tokens;   // R * T
 };
@@ -80,7 +81,8 @@ struct DispatchArgs {
   int64_t* recv_idx;
   float* recv_w;
   int32_t* recv_md;
-  int R, E, L, K, T, H, G, M, compact, zero_padding, n_so, n_su;
+  int R, E, L, K, T, H, G, M, compact, zero_padding, n_so, n_su, sf_pack;
+  int SW;  // 32-bit words of one row's scale sidecar
   int64_t region_rows;
   int64_t num_tokens;
   int in_row_bytes, out_row_bytes;
@@ -100,7 +102,7 @@ struct SortArgs {
   float* out_w;
   int32_t* out_md;
   const int32_t* send_counters;  // [R src][R dst]: rows each source sent each destination
-  int R, K, M, G, n_so, n_su;
+  int R, K, M, SW, n_so, n_su;
   int64_t region_rows;
   int row_bytes;
 };

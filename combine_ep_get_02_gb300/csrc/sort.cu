@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(kSortThreads) sort_kernel(SortArgs a) {
       }
     }
     if (a.in_sf != nullptr)
-      for (int g = lane; g < a.G; g += 32) a.out_sf[to * a.G + g] = a.in_sf[from * a.G + g];
+      for (int g = lane; g < a.SW; g += 32) a.out_sf[to * a.SW + g] = a.in_sf[from * a.SW + g];
     if (lane < a.K) {
       a.out_idx[to * a.K + lane] = a.in_idx[from * a.K + lane];
       a.out_w[to * a.K + lane] = a.in_w[from * a.K + lane];

@@ -86,6 +86,15 @@ typedef struct ep_config {
                                       rows between each expert's lanes and the next
                                       expert_alignment boundary (and their FP8
                                       scales); 0 = those rows are left untouched  */
+  int32_t sf_pack;                 /* FP8 receive only. 0: recv_sf row = G fp32 scales
+                                      (amax/448). 1: packed power-of-two scales (a
+                                      reading of [P690]'s num_sf_packs, whose format the
+                                      pages do not give): per 128 columns one byte
+                                      e+127 (UE8M0) with 2^e the smallest power of two
+                                      >= amax/448 and q = e4m3(x * 2^-e); four groups
+                                      per 32-bit word, group g in byte g%4 of word g/4,
+                                      so a row holds ceil(G/4) words. Pre-cast FP8
+                                      input then carries x_sf in the same packing.  */
 } ep_config_t;
 
 /* ---- dispatch layout (all device pointers, int32 unless noted) -------------
@@ -129,7 +138,8 @@ typedef struct ep_layout {
  */
 typedef struct ep_recv {
   void* recv_x;                /* [recv_x_rows][H] bf16 or e4m3                 */
-  float* recv_sf;              /* [recv_x_rows][H/128] (FP8 receive only)       */
+  float* recv_sf;              /* [recv_x_rows][H/128] fp32, or [recv_x_rows][ceil(H/512)]
+                                  packed words with sf_pack (FP8 receive only)   */
   int64_t* recv_topk_idx;      /* [R][R*M][K]: destination-local expert or -1    */
   float* recv_topk_weights;    /* [R][R*M][K]: weight, or 0 off this destination */
   int32_t* recv_src_metadata;  /* [R][R*M][2+K]: {src rank, src token,

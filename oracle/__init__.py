@@ -26,7 +26,7 @@ OK, INVALID, UNSUPPORTED, BAD_TOPK, OVERFLOW = 0, -1, -2, -5, -6
 class _Cfg(C.Structure):
     _fields_ = [(n, C.c_int32) for n in
                 ("n_so", "n_su", "E", "K", "T", "M", "H", "x_fp8", "recv_fp8", "expand", "align",
-                 "compact", "zero_padding")]
+                 "compact", "zero_padding", "sf_pack")]
 
 
 _lib = None
@@ -51,6 +51,7 @@ def lib():
         L.orc_e4m3_of_bits.argtypes = [C.c_uint32, C.c_int64, P]
         L.orc_bf16_of_bits.argtypes = [C.c_uint32, C.c_int64, P]
         L.orc_cast_row_fp8.argtypes = [P, C.c_int, P, P]
+        L.orc_cast_row_fp8_ue8m0.argtypes = [P, C.c_int, P, P]
         L.orc_recv_rows.restype = C.c_int64
         L.orc_recv_rows.argtypes = [P]
         L.orc_layout.restype = C.c_int
@@ -78,7 +79,8 @@ def cfg_of(wl) -> _Cfg:
                 wl.num_max_tokens_per_rank, wl.hidden, int(wl.x_dtype == "fp8"),
                 int(wl.recv_dtype == "fp8"), int(bool(wl.expand)), wl.expert_alignment,
                 int(bool(getattr(wl, "compact", False))),
-                int(bool(getattr(wl, "zero_padding", False))))
+                int(bool(getattr(wl, "zero_padding", False))),
+                int(bool(getattr(wl, "sf_pack", False))))
 
 
 def _np(a, dtype):
@@ -139,6 +141,22 @@ def bf16_of_bits(first: int, n: int) -> np.ndarray:
     return out
 
 
+def sf_words(wl) -> int:
+    """32-bit words of one row's scale sidecar: G fp32 scales, or ceil(G/4) packed words."""
+    G = wl.hidden // 128
+    return (G + 3) // 4 if getattr(wl, "sf_pack", False) else G
+
+
+def cast_row_fp8_ue8m0(x_bits: np.ndarray):
+    """Packed-exponent FP8 cast of one bf16 row: (codes uint8 [H], words uint32 [ceil(G/4)])."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    H = x.size
+    q = np.empty(H, np.uint8)
+    words = np.empty((H // 128 + 3) // 4, np.uint32)
+    lib().orc_cast_row_fp8_ue8m0(_p(x), H, _p(q), _p(words))
+    return q, words
+
+
 def cast_row_fp8(x_bits: np.ndarray):
     """FP8 cast of one bf16 row (given as uint16 bits): (codes uint8 [H], sf fp32 [H/128])."""
     x = np.ascontiguousarray(x_bits, dtype=np.uint16)
@@ -195,6 +213,7 @@ def dispatch_token(wl, lay, s, t, x_row, x_sf_row, idx_tok, w_tok):
     sfr = None if x_sf_row is None else np.ascontiguousarray(x_sf_row, dtype=np.float32)
     hid = np.zeros(H * 2, np.uint8)
     hid_sf = np.zeros(max(G, 1), np.float32)
+    SW = sf_words(wl)
     hid_dst = np.zeros(K, np.int32)
     hid_row = np.zeros(K, np.int64)
     meta_dst = np.zeros(K, np.int32)
@@ -211,7 +230,7 @@ def dispatch_token(wl, lay, s, t, x_row, x_sf_row, idx_tok, w_tok):
         _p(hid_row), _p(meta_dst), _p(meta_row), _p(meta_idx), _p(meta_w), _p(meta_md))
     n_hid, n_meta = n & 0xFF, n >> 8
     hid = hid[:H] if fp8_out else hid.view(np.uint16)[:H]
-    return dict(hid=hid, hid_sf=hid_sf[:G] if fp8_out else None,
+    return dict(hid=hid, hid_sf=hid_sf[:SW] if fp8_out else None,
                 hid_dst=hid_dst[:n_hid], hid_row=hid_row[:n_hid],
                 meta_dst=meta_dst[:n_meta], meta_row=meta_row[:n_meta],
                 meta_idx=meta_idx[:n_meta], meta_w=meta_w[:n_meta], meta_md=meta_md[:n_meta])
@@ -230,9 +249,10 @@ def dispatch(wl, lay, x, x_sf, topk_idx, topk_weights, fill=0):
     fp8_out = wl.recv_dtype == "fp8"
     xa = _np(x, np.uint8 if fp8_in else np.uint16)
     sfa = None if x_sf is None else _np(x_sf, np.float32)
+    SW = sf_words(wl)
     out = dict(
         recv_x=np.full((rows, H * (1 if fp8_out else 2)), fill, np.uint8).view(np.uint8 if fp8_out else np.uint16),
-        recv_sf=np.full((rows, G * 4), fill, np.uint8).view(np.float32) if fp8_out else None,
+        recv_sf=np.full((rows, SW * 4), fill, np.uint8).view(np.float32) if fp8_out else None,
         recv_topk_idx=np.zeros((R, R * M, K), np.int64),
         recv_topk_weights=np.zeros((R, R * M, K), np.float32),
         recv_src_metadata=np.zeros((R, R * M, 2 + K), np.int32),

@@ -52,7 +52,7 @@ namespace {
 
 struct Cfg {
   int32_t n_so, n_su, E, K, T, M, H;
-  int32_t x_fp8, recv_fp8, expand, align, compact, zero_padding;
+  int32_t x_fp8, recv_fp8, expand, align, compact, zero_padding, sf_pack;
 };
 
 constexpr int kOk = 0;
@@ -135,6 +135,34 @@ void cast_row_fp8(const uint16_t* x, int H, uint8_t* q, float* sf) {
   }
 }
 
+// Packed scales (reading of the pages' num_sf_packs, whose format they do not
+// give): per 128 columns an unsigned power-of-two exponent byte (UE8M0, value
+// 2^(byte - 127)); four groups per 32-bit word, group g in byte g % 4 of word
+// g / 4. The scale is the smallest power of two 2^e with amax <= 448 * 2^e
+// (amax clamped below at 1e-4), and q = e4m3_rn_satfinite(x * 2^-e).
+void cast_row_fp8_ue8m0(const uint16_t* x, int H, uint8_t* q, uint32_t* words) {
+  const int G = H / 128;
+  std::memset(words, 0, sizeof(uint32_t) * ((G + 3) / 4));
+  for (int g = 0; g < G; ++g) {
+    float amax = 0.0f;
+    for (int c = 0; c < 128; ++c) amax = std::fmax(amax, std::fabs(bf16_to_f32(x[g * 128 + c])));
+    amax = std::fmax(amax, 1e-4f);
+    int e2;
+    std::frexp(static_cast<double>(amax), &e2);
+    int e = e2 - 10;  // 448 * 2^(e2 - 10) < 2^(e2 - 1) <= amax: too small, step up
+    while (static_cast<double>(amax) > std::ldexp(448.0, e)) ++e;
+    words[g / 4] |= static_cast<uint32_t>(e + 127) << (8 * (g % 4));
+    const float down = std::ldexp(1.0f, -e);
+    for (int c = 0; c < 128; ++c) q[g * 128 + c] = f32_to_e4m3(bf16_to_f32(x[g * 128 + c]) * down);
+  }
+}
+
+// 32-bit words of one row's scale sidecar: G fp32 scales, or ceil(G/4) packed words.
+int sf_words(int H, int sf_pack) {
+  const int G = H / 128;
+  return sf_pack ? (G + 3) / 4 : G;
+}
+
 int ranks(const Cfg& c) { return c.n_so * c.n_su; }
 
 // Row block of source s inside every destination's region (R blocks of M rows).
@@ -154,6 +182,7 @@ int check_cfg(const Cfg& c) {
   if (c.x_fp8 && !c.recv_fp8) return kUnsupported;
   if (c.compact && c.expand) return kUnsupported;
   if (c.zero_padding && !c.expand) return kUnsupported;
+  if (c.sf_pack && !c.recv_fp8) return kUnsupported;
   return kOk;
 }
 
@@ -197,7 +226,7 @@ extern "C" {
 
 struct orc_cfg {
   int32_t n_so, n_su, E, K, T, M, H;
-  int32_t x_fp8, recv_fp8, expand, align, compact, zero_padding;
+  int32_t x_fp8, recv_fp8, expand, align, compact, zero_padding, sf_pack;
 };
 
 static Cfg to_cfg(const orc_cfg* p) {
@@ -235,6 +264,9 @@ void orc_bf16_of_bits(uint32_t first, int64_t n, uint16_t* out) {
   }
 }
 void orc_cast_row_fp8(const uint16_t* x, int H, uint8_t* q, float* sf) { cast_row_fp8(x, H, q, sf); }
+void orc_cast_row_fp8_ue8m0(const uint16_t* x, int H, uint8_t* q, uint32_t* words) {
+  cast_row_fp8_ue8m0(x, H, q, words);
+}
 
 // Number of rows the receive buffer needs: R regions of R*M rows (row form),
 // or the expanded upper bound R*T*K + E*(align-1).
@@ -351,7 +383,8 @@ int orc_layout(const orc_cfg* p, const int64_t* topk_idx, int32_t* num_tokens_pe
 // The receive rows of one source token (s, t), computed from that token's
 // inputs and its layout entries.
 //   hid      : the row as received (H bf16 values, or H e4m3 codes)
-//   hid_sf   : its G = H/128 fp32 scales (FP8 receive only)
+//   hid_sf   : its scale sidecar (FP8 receive only): G = H/128 fp32 scales, or
+//              ceil(G/4) words of packed exponent bytes
 //   hid_dst / hid_row : the n_hid (destination, row) pairs that receive the
 //              hidden row; row = slot (row form), its compact row, or the
 //              expanded position inside the destination's region
@@ -366,14 +399,16 @@ int orc_dispatch_token(const orc_cfg* p, int s, int t, const int32_t* slot_tok,
                        int32_t* hid_dst, int64_t* hid_row, int32_t* meta_dst, int64_t* meta_row,
                        int64_t* meta_idx, float* meta_w, int32_t* meta_md) {
   const Cfg c = to_cfg(p);
-  const int R = ranks(c), L = c.E / R, K = c.K, H = c.H, G = H / 128;
+  const int R = ranks(c), L = c.E / R, K = c.K, H = c.H;
   (void)R;
   int status = kOk;
 
   // the row as it is received
   if (c.x_fp8) {
     std::memcpy(hid, x_row, H);
-    std::memcpy(hid_sf, x_sf_row, sizeof(float) * G);
+    std::memcpy(hid_sf, x_sf_row, sizeof(uint32_t) * sf_words(H, c.sf_pack));
+  } else if (c.recv_fp8 && c.sf_pack) {
+    cast_row_fp8_ue8m0(static_cast<const uint16_t*>(x_row), H, hid, reinterpret_cast<uint32_t*>(hid_sf));
   } else if (c.recv_fp8) {
     cast_row_fp8(static_cast<const uint16_t*>(x_row), H, hid, hid_sf);
   } else {
@@ -422,7 +457,7 @@ int orc_dispatch_token(const orc_cfg* p, int s, int t, const int32_t* slot_tok,
 // Full dispatch into caller-provided receive buffers (only filled rows are
 // written; the rest are left as they are). recv_psum is needed for the
 // compact layout only.
-//   recv_x [recv_rows][H] (bf16 or e4m3); recv_sf [recv_rows][G] (FP8 only)
+//   recv_x [recv_rows][H] (bf16 or e4m3); recv_sf [recv_rows][sf words] (FP8 only)
 //   recv_topk_idx [R][R*M][K], recv_topk_weights [R][R*M][K],
 //   recv_src_metadata [R][R*M][2+K]
 // In the row form, destination d's rows start at d*R*M; expanded rows at
@@ -436,7 +471,7 @@ int orc_dispatch(const orc_cfg* p, const int32_t* slot_map, const int32_t* exp_p
   const Cfg c = to_cfg(p);
   int status = check_cfg(c);
   if (status != kOk) return status;
-  const int R = ranks(c), K = c.K, T = c.T, H = c.H, G = H / 128;
+  const int R = ranks(c), K = c.K, T = c.T, H = c.H, G = H / 128, SW = sf_words(H, c.sf_pack);
   const int64_t region_rows = static_cast<int64_t>(R) * c.M;
   const size_t in_eb = c.x_fp8 ? 1 : 2, out_eb = c.recv_fp8 ? 1 : 2;
 
@@ -452,7 +487,7 @@ int orc_dispatch(const orc_cfg* p, const int32_t* slot_map, const int32_t* exp_p
       for (int k = 0; k < K; ++k) lane_valid(c, topk_idx + tok * K, k, &status);
       const int n = orc_dispatch_token(
           p, s, t, slot_map + tok * K, c.expand ? exp_pos + tok * K : nullptr, recv_psum,
-          static_cast<const uint8_t*>(x) + tok * H * in_eb, x_sf ? x_sf + tok * G : nullptr,
+          static_cast<const uint8_t*>(x) + tok * H * in_eb, x_sf ? x_sf + tok * SW : nullptr,
           topk_idx + tok * K, topk_weights + tok * K, hid.data(), hid_sf.data(), hid_dst.data(),
           hid_row.data(), meta_dst.data(), meta_row.data(), meta_idx.data(), meta_w.data(),
           meta_md.data());
@@ -461,7 +496,7 @@ int orc_dispatch(const orc_cfg* p, const int32_t* slot_map, const int32_t* exp_p
         const int64_t row = c.expand ? exp_region[hid_dst[i]] + hid_row[i]
                                      : hid_dst[i] * region_rows + hid_row[i];
         std::memcpy(static_cast<uint8_t*>(recv_x) + row * H * out_eb, hid.data(), H * out_eb);
-        if (c.recv_fp8) std::memcpy(recv_sf + row * G, hid_sf.data(), sizeof(float) * G);
+        if (c.recv_fp8) std::memcpy(recv_sf + row * SW, hid_sf.data(), sizeof(float) * SW);
       }
       for (int i = 0; i < n_meta; ++i) {
         const int64_t row = meta_dst[i] * region_rows + meta_row[i];
@@ -483,7 +518,7 @@ int orc_dispatch(const orc_cfg* p, const int32_t* slot_map, const int32_t* exp_p
         const int64_t end = static_cast<int64_t>(exp_region[d]) + exp_base[d * (L + 1) + j + 1];
         for (int64_t row = first; row < end; ++row) {
           std::memset(static_cast<uint8_t*>(recv_x) + row * H * out_eb, 0, H * out_eb);
-          if (c.recv_fp8) std::memset(recv_sf + row * G, 0, sizeof(float) * G);
+          if (c.recv_fp8) std::memset(recv_sf + row * SW, 0, sizeof(float) * SW);
         }
       }
     }

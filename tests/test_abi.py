@@ -84,6 +84,8 @@ def test_workspace_bytes_closed_form(ep):
     (dict(compact_recv=1, expand=1), -2),     # expanded rows are packed already
     (dict(zero_padding=1), -2),               # only expanded blocks have padding
     (dict(zero_padding=3, expand=1), -1),
+    (dict(sf_pack=1), -2),                    # packed scales need an FP8 receive
+    (dict(sf_pack=2, recv_dtype=1), -1),
 ])
 def test_invalid_configs_are_rejected_before_any_launch(ep, bad, code):
     c = cfg(ep, **bad)

@@ -150,3 +150,49 @@ def test_fp8_cast_power_of_two_scaling_invariance(orc):
         q, sf = orc.cast_row_fp8(_bf16_bits(x * np.float32(2.0 ** p)))
         assert np.array_equal(q, q0)
         assert np.array_equal(sf, sf0 * np.float32(2.0 ** p))
+
+
+# ---- packed power-of-two scales (reading of num_sf_packs) -------------------
+
+def test_packed_cast_hand_worked_group(orc):
+    g = np.zeros(512, np.float32)
+    g[:4] = [1.0, -2.0, 0.5, 0.0]
+    q, words = orc.cast_row_fp8_ue8m0(_bf16_bits(g))
+    # group 0: amax 2 -> 2/448 lies in (2^-8, 2^-7] -> e = -7, byte 120 = 0x78;
+    # q = x * 2^7: 128 -> 0x70, -256 -> 0xF8, 64 -> 0x68.
+    # groups 1..3 are zero: amax clamps to 1e-4, 1e-4/448 in (2^-23, 2^-22] -> 0x69
+    assert q[:4].tolist() == [0x70, 0xF8, 0x68, 0x00]
+    assert words.tolist() == [0x69696978]
+
+
+def test_packed_cast_properties(orc):
+    rng = np.random.default_rng(5)
+    H = 1152  # 9 groups: the third word holds one group and three zero bytes
+    for trial in range(30):
+        x = (rng.standard_normal(H) * 10.0 ** rng.uniform(-5, 5)).astype(np.float32)
+        xb = _bf16_bits(x)
+        xf = orc.bf16_to_f32(xb).astype(np.float64)
+        q, words = orc.cast_row_fp8_ue8m0(xb)
+        assert words.size == 3
+        b = words.view(np.uint8)  # little-endian: group g is byte g
+        assert not b[9:].any()
+        e = b[:9].astype(np.int64) - 127
+        amax = np.maximum(np.abs(xf).reshape(9, 128).max(1), np.float64(np.float32(1e-4)))
+        # the smallest power of two at or above amax / 448
+        assert np.all(amax <= 448.0 * 2.0 ** e) and np.all(amax > 448.0 * 2.0 ** (e - 1))
+        deq = orc.e4m3_to_f32(q).astype(np.float64).reshape(9, 128) * (2.0 ** e)[:, None]
+        err = np.abs(deq - xf.reshape(9, 128))
+        assert np.all(err <= 2.0 ** -4 * np.abs(xf.reshape(9, 128)) + 2.0 ** -10 * (2.0 ** e)[:, None])
+        assert np.all((q & 0x7F) <= 0x7E)
+
+
+def test_packed_cast_equals_fp32_cast_when_the_scale_is_a_power_of_two(orc):
+    # amax = 448 * 2^-3 = 56: the fp32 scale amax/448 is exactly 2^-3 = the packed one
+    rng = np.random.default_rng(9)
+    x = np.clip(rng.standard_normal(256).astype(np.float32) * 10, -55, 55)
+    x[7], x[200] = 56.0, -56.0
+    xb = _bf16_bits(x)
+    q1, sf = orc.cast_row_fp8(xb)
+    q2, words = orc.cast_row_fp8_ue8m0(xb)
+    assert np.all(sf == np.float32(0.125)) and words.view(np.uint8)[:2].tolist() == [124, 124]
+    assert np.array_equal(q1, q2)

@@ -48,6 +48,7 @@ class Workload:
     expert_alignment: int = 1
     compact: bool = False         # compact receive rows (row form only)
     zero_padding: bool = False    # zero the alignment padding rows (expanded only)
+    sf_pack: bool = False         # packed power-of-two scales, 4 per 32-bit word
     routing: str = "gauss"        # "gauss" | "zipf" | "hot"
     zipf_s: float = 1.1
     mask_frac: float = 0.0
@@ -102,6 +103,12 @@ PARITY = {
         name="direct_zipf_compact", compact=True, num_tokens=300, num_max_tokens_per_rank=320),
     "hybrid_compact": WORKLOADS["hybrid_rowform"].replace(
         name="hybrid_compact", compact=True, num_tokens=300, num_max_tokens_per_rank=300),
+    # packed power-of-two scales (fused cast, and pre-cast input carrying them)
+    "dsv3_fp8_packed": WORKLOADS["dsv3_fp8"].replace(
+        name="dsv3_fp8_packed", sf_pack=True, num_tokens=288, num_max_tokens_per_rank=288),
+    "precast_packed_h1152": WORKLOADS["dsv3_fp8"].replace(
+        name="precast_packed_h1152", x_dtype="fp8", sf_pack=True, hidden=1152, num_tokens=300,
+        num_max_tokens_per_rank=300),
     # expanded blocks aligned to 128 rows with zeroed padding
     "expanded_a128_zero": WORKLOADS["expanded"].replace(
         name="expanded_a128_zero", expert_alignment=128, zero_padding=True, num_tokens=100,
@@ -187,7 +194,14 @@ def hidden(wl: Workload):
     codes = torch.randint(0, 256, (R, T, H), generator=g, dtype=torch.int64).to(torch.uint8)
     nan = (codes & 0x7F) == 0x7F
     codes = torch.where(nan, codes ^ 1, codes)
-    sf = (torch.rand(R, T, H // 128, generator=g) * 1e-2 + 1e-3).to(torch.float32)
+    G = H // 128
+    if wl.sf_pack:  # exponent bytes 100..140, four per 32-bit word, zero past the last group
+        b = torch.randint(100, 141, (R, T, (G + 3) // 4 * 4), generator=g, dtype=torch.int64)
+        b[..., G:] = 0
+        words = (b[..., 0::4] | b[..., 1::4] << 8 | b[..., 2::4] << 16 | b[..., 3::4] << 24)
+        sf = words.to(torch.int64).to(torch.int32).view(torch.float32)
+        return codes.contiguous(), sf.contiguous()
+    sf = (torch.rand(R, T, G, generator=g) * 1e-2 + 1e-3).to(torch.float32)
     return codes.contiguous(), sf.contiguous()
 
 
