@@ -25,23 +25,46 @@ __global__ void __launch_bounds__(kCopyThreads) combine_kernel(CombineArgs a) {
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
   const int nchunk = a.H >> 3;  // 8 bf16 per chunk
 
-  for (int64_t tok = gwarp; tok < a.num_tokens; tok += nwarps) {
+  // A work unit is one token's column range (a token is split into a.splits
+  // ranges of a.split_chunks 16-byte chunks when tokens are too few to keep
+  // every warp busy to the end). Lane k of the warp carries top-k lane k of
+  // the unit's token; the next unit's routing (expert, slot or position,
+  // weight) is loaded while the current unit's rows stream.
+  const int64_t units = a.num_tokens * a.splits;
+  int64_t e_next = -1;
+  int r_next = -1;
+  float w_next = 0.f;
+  auto load_raw = [&](int64_t unit) {
+    e_next = -1;
+    r_next = -1;
+    w_next = 0.f;
+    if (unit < units && lane < a.K) {
+      const int64_t i = (unit / a.splits) * a.K + lane;
+      e_next = __ldg(a.topk_idx + i);
+      r_next = __ldg((kExpand ? a.exp_pos : a.slot_map) + i);
+      w_next = __ldg(a.topk_w + i);
+    }
+  };
+  load_raw(gwarp);
+  for (int64_t unit = gwarp; unit < units; unit += nwarps) {
+    const int64_t tok = unit / a.splits;
+    const int c_begin = static_cast<int>(unit - tok * a.splits) * a.split_chunks;
+    const int c_end = min(nchunk, c_begin + a.split_chunks);
+    const int64_t e = e_next;
+    const int r = r_next;
+    const float w_cur = w_next;
+    load_raw(unit + nwarps);
     if (lane < kMaxK) {
       const uint16_t* p = nullptr;
       float w = 0.f;
-      if (lane < a.K) {
-        const int64_t i = tok * a.K + lane;
-        const int64_t e = a.topk_idx[i];
-        const int r = kExpand ? a.exp_pos[i] : a.slot_map[i];
-        if (e >= 0 && e < a.E && r >= 0) {
-          const int d = static_cast<int>(e) / a.L;
-          const int64_t row =
-              kExpand ? static_cast<int64_t>(a.exp_region[d]) + r
-                      : static_cast<int64_t>(d) * a.region_rows +
-                            recv_row_of_slot(r, d, a.R, a.M, a.compact, a.recv_psum);
-          p = a.y + row * a.H;
-          w = a.topk_w[i];
-        }
+      if (e >= 0 && e < a.E && r >= 0) {
+        const int d = static_cast<int>(e) / a.L;
+        const int64_t row =
+            kExpand ? static_cast<int64_t>(a.exp_region[d]) + r
+                    : static_cast<int64_t>(d) * a.region_rows +
+                          recv_row_of_slot(r, d, a.R, a.M, a.compact, a.recv_psum);
+        p = a.y + row * a.H;
+        w = w_cur;
       }
       s_ptr[warp][lane] = p;
       s_w[warp][lane] = w;
@@ -55,19 +78,19 @@ __global__ void __launch_bounds__(kCopyThreads) combine_kernel(CombineArgs a) {
       wk[k] = s_w[warp][k];
     }
     uint16_t* orow = a.out + tok * a.H;
-    for (int c0 = lane; c0 < nchunk; c0 += 32 * kSteps) {
+    for (int c0 = c_begin + lane; c0 < c_end; c0 += 32 * kSteps) {
       uint4 v[kSteps][kMaxK];
 #pragma unroll
       for (int h = 0; h < kSteps; ++h) {
         const int c = c0 + h * 32;
 #pragma unroll
         for (int k = 0; k < kMaxK; ++k)
-          if (ptr[k] != nullptr && c < nchunk) v[h][k] = ld_ro16(ptr[k] + (static_cast<size_t>(c) << 3));
+          if (ptr[k] != nullptr && c < c_end) v[h][k] = ld_ro16(ptr[k] + (static_cast<size_t>(c) << 3));
       }
 #pragma unroll
       for (int h = 0; h < kSteps; ++h) {
         const int c = c0 + h * 32;
-        if (c >= nchunk) continue;
+        if (c >= c_end) continue;
         float acc[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = 0.f;
@@ -90,19 +113,32 @@ __global__ void __launch_bounds__(kCopyThreads) combine_kernel(CombineArgs a) {
         st16(orow + (static_cast<size_t>(c) << 3), o);
       }
     }
-    __syncwarp();  // s_ptr / s_w are rewritten by the next token
+    __syncwarp();  // s_ptr / s_w are rewritten by the next unit
   }
 }
 
 template <bool kExpand, int kMaxK, int kSteps>
-cudaError_t launch_one(const CombineArgs& a, int num_sms, cudaStream_t stream) {
+cudaError_t launch_one(const CombineArgs& args, int num_sms, cudaStream_t stream) {
   auto kern = combine_kernel<kExpand, kMaxK, kSteps>;
   int per_sm = 0;
   cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kCopyThreads, 0);
   if (err != cudaSuccess) return err;
   if (per_sm < 1) per_sm = 1;
+  CombineArgs a = args;
+  // Split tokens into column ranges until every warp gets about 16 units, so
+  // that the last wave is short; a range is a whole number of lane sweeps.
+  const int64_t warps = static_cast<int64_t>(num_sms) * per_sm * kWarps;
+  const int nchunk = a.H >> 3;
+  const int sweep = 32 * kSteps;
+  const int max_splits = (nchunk + sweep - 1) / sweep;
+  int64_t want = a.num_tokens > 0 ? (16 * warps + a.num_tokens - 1) / a.num_tokens : 1;
+  if (want > max_splits) want = max_splits;
+  if (want < 1) want = 1;
+  a.split_chunks = static_cast<int>(((nchunk + want - 1) / want + sweep - 1) / sweep * sweep);
+  a.splits = (nchunk + a.split_chunks - 1) / a.split_chunks;
+  if (a.splits < 1) a.splits = 1;
   int64_t ctas = static_cast<int64_t>(num_sms) * per_sm;
-  const int64_t need = (a.num_tokens + kWarps - 1) / kWarps;
+  const int64_t need = (a.num_tokens * a.splits + kWarps - 1) / kWarps;
   if (ctas > need) ctas = need;
   if (ctas < 1) return cudaSuccess;
   kern<<<static_cast<unsigned>(ctas), kCopyThreads, 0, stream>>>(a);

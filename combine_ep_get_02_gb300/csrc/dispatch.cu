@@ -16,7 +16,8 @@ namespace ep {
 namespace {
 
 constexpr int kWarps = kCopyThreads / 32;
-constexpr int kUnroll = 4;  // 16-byte chunks in flight per lane
+constexpr int kUnroll = 4;     // 16-byte chunks in flight per lane (row copy)
+constexpr int kCastUnits = 4;  // 16-column units in flight per lane (cast)
 
 enum Kind { kCopyRow = 0, kCastRow = 1 };
 
@@ -28,27 +29,43 @@ struct TokenLanes {
   unsigned rmask;  // first lane per destination (deduplicated entries)
 };
 
+// The raw routing of top-k lane `lane` of a token, loaded one token ahead.
+struct RawLane {
+  int64_t e;
+  int slot, pos;
+  float w;
+};
+
+__device__ __forceinline__ RawLane fetch_lane(const DispatchArgs& a, int64_t tok, int lane, bool expand,
+                                              bool atomic) {
+  RawLane r;
+  r.e = -1;
+  r.slot = -1;
+  r.pos = -1;
+  r.w = 0.f;
+  if (tok < a.num_tokens && lane < a.K) {
+    const int64_t i = tok * a.K + lane;
+    r.e = __ldg(a.topk_idx + i);
+    if (!atomic) r.slot = __ldg(a.slot_map + i);
+    r.w = __ldg(a.topk_w + i);
+    if (expand) r.pos = __ldg(a.exp_pos + i);
+  }
+  return r;
+}
+
 // Lane k < K: the token's k-th top-k lane. Invalid lanes get a distinct
 // negative d so that they never group with anything. With `atomic` (the
 // prior-art comparison path) there is no layout: the first lane to each
 // destination takes the next row of the source's block with an atomicAdd on
 // the (source, destination) counter, so the order inside a block depends on
 // which warp gets there first (PR #753, Motivation).
-__device__ __forceinline__ TokenLanes load_lanes(const DispatchArgs& a, int64_t tok, int lane,
-                                                 bool expand, bool atomic = false) {
+__device__ __forceinline__ TokenLanes lanes_of(const DispatchArgs& a, const RawLane& raw, int64_t tok,
+                                               int lane, bool expand, bool atomic) {
   TokenLanes L;
-  L.e = -1;
-  L.slot = -1;
-  L.pos = -1;
-  L.w = 0.f;
-  if (lane < a.K) {
-    const int64_t i = tok * a.K + lane;
-    const int64_t e = a.topk_idx[i];
-    if (!atomic) L.slot = a.slot_map[i];
-    L.w = a.topk_w[i];
-    if (expand) L.pos = a.exp_pos[i];
-    L.e = (e >= 0 && e < a.E) ? static_cast<int>(e) : -1;
-  }
+  L.slot = raw.slot;
+  L.pos = raw.pos;
+  L.w = raw.w;
+  L.e = (raw.e >= 0 && raw.e < a.E) ? static_cast<int>(raw.e) : -1;
   const bool valid = L.e >= 0 && (atomic || (expand ? L.pos >= 0 : L.slot >= 0));
   L.d = valid ? L.e / a.L : -1 - lane;
   const unsigned same = __match_any_sync(kFullMask, L.d);
@@ -75,10 +92,14 @@ __global__ void __launch_bounds__(kCopyThreads) dispatch_kernel(DispatchArgs a) 
   const int64_t gwarp = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
 
+  // the next token's routing loads while this token's row streams
+  RawLane next = fetch_lane(a, gwarp, lane, kExpand, kAtomic);
   for (int64_t tok = gwarp; tok < a.num_tokens; tok += nwarps) {
     const int s = static_cast<int>(tok / a.T);
     const int t = static_cast<int>(tok - static_cast<int64_t>(s) * a.T);
-    const TokenLanes ln = load_lanes(a, tok, lane, kExpand, kAtomic);
+    const RawLane cur = next;
+    next = fetch_lane(a, tok + nwarps, lane, kExpand, kAtomic);
+    const TokenLanes ln = lanes_of(a, cur, tok, lane, kExpand, kAtomic);
     const unsigned hmask = kExpand ? ln.vmask : ln.rmask;
     if ((hmask >> lane) & 1) {
       const int64_t row = kExpand ? static_cast<int64_t>(a.exp_region[ln.d]) + ln.pos
@@ -120,10 +141,10 @@ __global__ void __launch_bounds__(kCopyThreads) dispatch_kernel(DispatchArgs a) 
       // (32 bytes in, 16 bytes out); 8 consecutive lanes form one 128-column group.
       const uint8_t* src = a.x + tok * a.in_row_bytes;
       const int nunit = a.H >> 4;  // multiple of 8
-      for (int u0 = 0; u0 < nunit; u0 += 32 * 2) {
-        uint4 lo[2], hi[2];
+      for (int u0 = 0; u0 < nunit; u0 += 32 * kCastUnits) {
+        uint4 lo[kCastUnits], hi[kCastUnits];
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
+        for (int r = 0; r < kCastUnits; ++r) {
           const int u = u0 + r * 32 + lane;
           if (u < nunit) {
             lo[r] = ld_stream16(src + (static_cast<size_t>(u) << 5));
@@ -131,7 +152,7 @@ __global__ void __launch_bounds__(kCopyThreads) dispatch_kernel(DispatchArgs a) 
           }
         }
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
+        for (int r = 0; r < kCastUnits; ++r) {
           const int u = u0 + r * 32 + lane;
           if (u0 + r * 32 >= nunit) continue;  // warp-uniform
           float f[16];

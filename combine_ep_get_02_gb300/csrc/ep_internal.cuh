@@ -117,6 +117,8 @@ struct CombineArgs {
   const int32_t* recv_psum;  // compact receive rows only
   uint16_t* out;
   int E, L, K, T, H, R, M, compact;
+  int splits;        // column ranges per token (work units per token)
+  int split_chunks;  // 16-byte chunks per range
   int64_t region_rows;
   int64_t num_tokens;
 };

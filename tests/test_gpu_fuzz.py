@@ -72,8 +72,10 @@ def test_fuzz_case(seed):
     st, orec = oracle.dispatch(wl, olay, x, sf, idx, w, fill=0xFF)
     assert st == 0
     rows = int(olay["exp_region"][-1]) if wl.expand else orec["recv_x"].shape[0]
-    got = run.recv.recv_x[:rows].contiguous().view(torch.uint8).cpu().numpy()
-    assert np.array_equal(got, orec["recv_x"][:rows].reshape(rows, -1).view(np.uint8)), wl
+    row_bytes = wl.hidden * (1 if wl.recv_dtype == "fp8" else 2)
+    got = run.recv.recv_x[:rows].contiguous().view(torch.uint8).cpu().numpy().reshape(rows, row_bytes)
+    exp = np.ascontiguousarray(orec["recv_x"][:rows]).view(np.uint8).reshape(rows, row_bytes)
+    assert np.array_equal(got, exp), wl
     if wl.recv_dtype == "fp8":
         got_sf = run.recv.recv_sf[:rows].cpu().numpy().view(np.uint32)
         assert np.array_equal(got_sf, orec["recv_sf"][:rows].view(np.uint32)), wl
