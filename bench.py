@@ -423,11 +423,7 @@ def ncu_traffic(kernel, wl, n_tok):
         return None
     try:
         from combine_ep_get_02_gb300 import _build
-        import hashlib
-        h = hashlib.sha256()
-        for p in _build.sources():
-            h.update(open(p, "rb").read())
-        src = h.hexdigest()[:16]
+        src = _build.source_hash()
         for line in open(path):
             f = line.split()
             if len(f) == 6 and f[0] == kernel and f[1] == wl.name and f[5] == src:

@@ -37,6 +37,17 @@ def _deps():
     return sources() + hdr + [os.path.abspath(__file__)]
 
 
+def source_hash() -> str:
+    """Short hash of every kernel source and header (identifies a build's kernels)."""
+    import hashlib
+    h = hashlib.sha256()
+    for p in sorted(_deps()):
+        if p.endswith((".cu", ".cuh", ".h")):
+            h.update(os.path.basename(p).encode())
+            h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
 def up_to_date() -> bool:
     if not os.path.exists(LIB):
         return False

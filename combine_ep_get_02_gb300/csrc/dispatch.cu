@@ -8,6 +8,7 @@
 // racing for them). Tokens are spread over a persistent grid sized to the SMs.
 // Lanes 0..K-1 carry the token's top-k lanes and write the small sidecar rows
 // (routing of the lanes to that destination and the source metadata).
+#include "dispatch_common.cuh"
 #include "ep_device.cuh"
 #include "ep_internal.cuh"
 
@@ -20,68 +21,6 @@ constexpr int kUnroll = 4;     // 16-byte chunks in flight per lane (row copy)
 constexpr int kCastUnits = 4;  // 16-column units in flight per lane (cast)
 
 enum Kind { kCopyRow = 0, kCastRow = 1 };
-
-struct TokenLanes {
-  int e, d, slot, pos;
-  int row;  // receive row of the lane's deduplicated entry inside its destination region
-  float w;
-  unsigned vmask;  // valid lanes
-  unsigned rmask;  // first lane per destination (deduplicated entries)
-};
-
-// The raw routing of top-k lane `lane` of a token, loaded one token ahead.
-struct RawLane {
-  int64_t e;
-  int slot, pos;
-  float w;
-};
-
-__device__ __forceinline__ RawLane fetch_lane(const DispatchArgs& a, int64_t tok, int lane, bool expand,
-                                              bool atomic) {
-  RawLane r;
-  r.e = -1;
-  r.slot = -1;
-  r.pos = -1;
-  r.w = 0.f;
-  if (tok < a.num_tokens && lane < a.K) {
-    const int64_t i = tok * a.K + lane;
-    r.e = __ldg(a.topk_idx + i);
-    if (!atomic) r.slot = __ldg(a.slot_map + i);
-    r.w = __ldg(a.topk_w + i);
-    if (expand) r.pos = __ldg(a.exp_pos + i);
-  }
-  return r;
-}
-
-// Lane k < K: the token's k-th top-k lane. Invalid lanes get a distinct
-// negative d so that they never group with anything. With `atomic` (the
-// prior-art comparison path) there is no layout: the first lane to each
-// destination takes the next row of the source's block with an atomicAdd on
-// the (source, destination) counter, so the order inside a block depends on
-// which warp gets there first (PR #753, Motivation).
-__device__ __forceinline__ TokenLanes lanes_of(const DispatchArgs& a, const RawLane& raw, int64_t tok,
-                                               int lane, bool expand, bool atomic) {
-  TokenLanes L;
-  L.slot = raw.slot;
-  L.pos = raw.pos;
-  L.w = raw.w;
-  L.e = (raw.e >= 0 && raw.e < a.E) ? static_cast<int>(raw.e) : -1;
-  const bool valid = L.e >= 0 && (atomic || (expand ? L.pos >= 0 : L.slot >= 0));
-  L.d = valid ? L.e / a.L : -1 - lane;
-  const unsigned same = __match_any_sync(kFullMask, L.d);
-  L.vmask = __ballot_sync(kFullMask, valid);
-  L.rmask = __ballot_sync(kFullMask, valid && (same & lanemask_lt()) == 0);
-  if (atomic) {
-    const int s = static_cast<int>(tok / a.T);
-    const int rb = a.n_so == 1 ? s : (s % a.n_su) * a.n_so + s / a.n_su;
-    int mine = -1;
-    if ((L.rmask >> lane) & 1) mine = rb * a.M + atomicAdd(a.send_counters + s * a.R + L.d, 1);
-    L.slot = __shfl_sync(kFullMask, mine, __ffs(same) - 1);
-    if (!valid) L.slot = -1;
-  }
-  L.row = (valid && !expand) ? recv_row_of_slot(L.slot, L.d, a.R, a.M, a.compact, a.recv_psum) : -1;
-  return L;
-}
 
 template <int kKind, bool kExpand, bool kAtomic = false>
 __global__ void __launch_bounds__(kCopyThreads) dispatch_kernel(DispatchArgs a) {
@@ -155,39 +94,12 @@ __global__ void __launch_bounds__(kCopyThreads) dispatch_kernel(DispatchArgs a) 
         for (int r = 0; r < kCastUnits; ++r) {
           const int u = u0 + r * 32 + lane;
           if (u0 + r * 32 >= nunit) continue;  // warp-uniform
-          float f[16];
-          const uint32_t wv[8] = {lo[r].x, lo[r].y, lo[r].z, lo[r].w, hi[r].x, hi[r].y, hi[r].z, hi[r].w};
-          float amax = 0.f;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float2 p = bf16x2_to_f32x2(u < nunit ? wv[i] : 0u);
-            f[2 * i] = p.x;
-            f[2 * i + 1] = p.y;
-            amax = fmaxf(amax, fmaxf(fabsf(p.x), fabsf(p.y)));
-          }
-          amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
-          amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 2));
-          amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 4));
-          amax = fmaxf(amax, 1e-4f);
-          // fp32 scale: inv = 448/amax. Packed: the smallest 2^e >= amax/448, read off
-          // amax's exponent and mantissa (amax = m*2^k; e = k-8, or k-7 when m > 1.75).
-          const uint32_t ab = __float_as_uint(amax);
-          const int e2 = static_cast<int>(ab >> 23) - 127 - 8 + ((ab & 0x7FFFFFu) > 0x600000u ? 1 : 0);
-          const float inv = a.sf_pack ? __uint_as_float(static_cast<uint32_t>(127 - e2) << 23)
-                                      : __fdiv_rn(448.0f, amax);
-          uint4 q;
-          q.x = f32x2_to_e4m3x2(__fmul_rn(f[0], inv), __fmul_rn(f[1], inv)) |
-                f32x2_to_e4m3x2(__fmul_rn(f[2], inv), __fmul_rn(f[3], inv)) << 16;
-          q.y = f32x2_to_e4m3x2(__fmul_rn(f[4], inv), __fmul_rn(f[5], inv)) |
-                f32x2_to_e4m3x2(__fmul_rn(f[6], inv), __fmul_rn(f[7], inv)) << 16;
-          q.z = f32x2_to_e4m3x2(__fmul_rn(f[8], inv), __fmul_rn(f[9], inv)) |
-                f32x2_to_e4m3x2(__fmul_rn(f[10], inv), __fmul_rn(f[11], inv)) << 16;
-          q.w = f32x2_to_e4m3x2(__fmul_rn(f[12], inv), __fmul_rn(f[13], inv)) |
-                f32x2_to_e4m3x2(__fmul_rn(f[14], inv), __fmul_rn(f[15], inv)) << 16;
+          const CastUnit cu = cast_unit(lo[r], hi[r], u < nunit, a.sf_pack);
+          const uint4 q = cu.q;
           if (u < nunit) {
             if ((lane & 7) == 0) {
-              if (a.sf_pack) reinterpret_cast<uint8_t*>(s_sf[warp])[u >> 3] = static_cast<uint8_t>(e2 + 127);
-              else s_sf[warp][u >> 3] = __fdiv_rn(amax, 448.0f);
+              if (a.sf_pack) reinterpret_cast<uint8_t*>(s_sf[warp])[u >> 3] = cu.sf_byte;
+              else s_sf[warp][u >> 3] = cu.sf;
             }
             for (int j = 0; j < nh; ++j)
               st16(a.recv_x + s_row[warp][j] * a.out_row_bytes + (static_cast<size_t>(u) << 4), q);
@@ -213,60 +125,12 @@ __global__ void __launch_bounds__(kCopyThreads) dispatch_kernel(DispatchArgs a) 
       }
     }
 
-    // sidecar rows of each deduplicated destination (row form). Metadata field
-    // f = 2 + k carries lane k's expanded row; with K up to 32 there are up to 34
-    // fields, so a lane writes fields lane and lane + 32.
-    if (a.recv_idx != nullptr || a.recv_w != nullptr || a.recv_md != nullptr) {
-      const int f0_d = __shfl_sync(kFullMask, ln.d, (lane - 2) & 31);   // lane f-2 for f = lane
-      const int f0_pos = __shfl_sync(kFullMask, ln.pos, (lane - 2) & 31);
-      const int f1_d = __shfl_sync(kFullMask, ln.d, (lane + 30) & 31);  // f = lane + 32
-      const int f1_pos = __shfl_sync(kFullMask, ln.pos, (lane + 30) & 31);
-      unsigned m = ln.rmask;
-      while (m) {
-        const int rl = __ffs(m) - 1;
-        m &= m - 1;
-        const int dj = __shfl_sync(kFullMask, ln.d, rl);
-        const int row = __shfl_sync(kFullMask, kExpand ? ln.slot : ln.row, rl);
-        const int64_t mrow = static_cast<int64_t>(dj) * a.region_rows + row;
-        if (lane < a.K) {
-          const bool on = ln.d == dj;
-          if (a.recv_idx) a.recv_idx[mrow * a.K + lane] = on ? static_cast<int64_t>(ln.e - dj * a.L) : -1;
-          if (a.recv_w) a.recv_w[mrow * a.K + lane] = on ? ln.w : 0.f;
-        }
-        if (a.recv_md) {
-          int32_t* md = a.recv_md + mrow * (a.K + 2);
-          if (lane < a.K + 2) {
-            int v;
-            if (lane == 0) v = s;
-            else if (lane == 1) v = t;
-            else v = (kExpand && f0_d == dj) ? f0_pos : -1;
-            md[lane] = v;
-          }
-          if (lane + 32 < a.K + 2) md[lane + 32] = (kExpand && f1_d == dj) ? f1_pos : -1;
-        }
-      }
-    }
+    write_sidecars(a, ln, s, t, lane, kExpand);
     __syncwarp();  // s_row / s_sf are rewritten by the next token
   }
 
-  // expanded blocks padded to expert_alignment: zero the rows after each
-  // expert's lanes up to the next block start (and their scales)
-  if (kExpand && a.zero_padding) {
-    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-    const int nchunk = a.out_row_bytes >> 4;
-    for (int64_t blk = gwarp; blk < a.E; blk += nwarps) {
-      const int d = static_cast<int>(blk / a.L), j = static_cast<int>(blk % a.L);
-      const int64_t region = a.exp_region[d];
-      const int64_t first = region + a.exp_base[d * (a.L + 1) + j] + a.exp_cnt[blk];
-      const int64_t end = region + a.exp_base[d * (a.L + 1) + j + 1];
-      for (int64_t row = first; row < end; ++row) {
-        uint8_t* dst = a.recv_x + row * a.out_row_bytes;
-        for (int c = lane; c < nchunk; c += 32) st16(dst + (static_cast<size_t>(c) << 4), zero);
-        if (kKind == kCastRow || a.x_sf != nullptr)
-          for (int g = lane; g < a.SW; g += 32) a.recv_sf[row * a.SW + g] = 0.f;
-      }
-    }
-  }
+  if (kExpand && a.zero_padding)
+    zero_padding_rows(a, gwarp, nwarps, lane, kKind == kCastRow || a.x_sf != nullptr);
 }
 
 template <int kKind, bool kExpand, bool kAtomic = false>
