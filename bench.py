@@ -54,6 +54,7 @@ def parse():
                    help="time dispatch + combine only, replaying a layout computed once")
     p.add_argument("--compare-sort", action="store_true",
                    help="time the deterministic dispatch against atomic slots + post-hoc sort")
+    p.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline sample")
@@ -294,6 +295,10 @@ def native(args):
     gbs = {k: abytes[k] / (phase_ms[k] * 1e-3) / 1e9 for k in abytes}
     dominant = max(("dispatch", "combine"), key=lambda k: phase_ms[k])
 
+    graph = None
+    if not args.no_graph and not args.cached:
+        graph = graph_replay(ep, cfg, idx, lay, ws, x, sf, w, recv, y, out, stream, dev, args, world, R * T)
+
     e2e = None
     if not args.no_e2e:
         e2e = end_to_end(ep, cfg, wl, idx_h, w_h, x_h, sf_h, lay, recv, y, identity, ws, stream, dev,
@@ -323,12 +328,14 @@ def native(args):
                 "frac_of_peak": gbs[k] / peak} for k in ("layout", "dispatch", "combine")},
         "roofline": {"kernel": f"{dominant}_kernel", "bound": "hbm", "achieved": gbs[dominant],
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": gbs[dominant] / peak, "traffic": ncu_traffic(dominant, wl, R * T)},
+                     "frac": gbs[dominant] / peak, "traffic": ncu_traffic(f"{dominant}_kernel", wl, R * T)},
         "clocks": clocks.summary(),
         "gpu_launches": args.steps * launches_per_step(wl, args.cached),
     }
     if e2e is not None:
         line["e2e"] = e2e
+    if graph is not None:
+        line["graph"] = graph
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, idx_h, w_h, x_h, sf_h, y, args.cpu_seconds)
     if rank == 0:
@@ -336,6 +343,32 @@ def native(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def graph_replay(ep, cfg, idx, lay, ws, x, sf, w, recv, y, out, stream, dev, args, world, units):
+    """The same step captured once as a CUDA graph (its launches with no host work
+    between them) and replayed: steps per second without launch gaps."""
+    cs = torch.cuda.Stream(dev)
+    cs.wait_stream(stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cs), torch.cuda.graph(g, stream=cs):
+        ep.ep_get_dispatch_layout(cfg, idx, lay, ws, cs)
+        ep.ep_dispatch(cfg, lay, x, sf, idx, w, recv, ws, cs)
+        ep.ep_combine(cfg, lay, y, idx, w, out, ws, cs)
+    for _ in range(max(args.warmup, 1)):
+        g.replay()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        g.replay()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(world, a.elapsed_time(b))
+    return {"ms_per_step": ms / args.steps, "value": whole_job_rate(world, units, ms, args.steps),
+            "unit": "tokens/s"}
 
 
 def launches_per_step(wl, cached=False):

@@ -301,3 +301,38 @@ def test_atomic_slots_plus_sort_equal_the_deterministic_dispatch(name):
         if a is None:
             continue
         assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), f
+
+
+@pytest.mark.parametrize("name", ["dsv3_fp8", "expanded", "hybrid_compact"])
+def test_cuda_graph_replay_equals_eager(name):
+    """layout -> dispatch -> combine captured once in a CUDA graph and replayed
+    gives the eager results bit for bit (the workspace counter returns to zero
+    inside every replay)."""
+    wl = W.PARITY[name]
+    idx, w, x, sf = inputs(wl)
+    eager = GpuRun(wl, idx, w, x, sf).layout().dispatch()
+    y = eager.recv.recv_x if (wl.recv_dtype == "bf16" and not wl.expand) else \
+        random_y(wl, ep.ep_recv_rows(eager.cfg), eager.dev)
+    eager.combine(y)
+    assert eager.status() == ep.EP_OK
+    run = GpuRun(wl, idx, w, x, sf)
+    run.recv = ep.alloc_recv(run.cfg, run.dev, zero=True)
+    run.out = torch.empty_like(eager.out)
+    y2 = run.recv.recv_x if (wl.recv_dtype == "bf16" and not wl.expand) else y
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        ep.ep_get_dispatch_layout(run.cfg, run.idx, run.lay, run.ws, s)  # first call outside capture
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            ep.ep_get_dispatch_layout(run.cfg, run.idx, run.lay, run.ws, s)
+            ep.ep_dispatch(run.cfg, run.lay, run.x, run.sf, run.idx, run.w, run.recv, run.ws, s)
+            ep.ep_combine(run.cfg, run.lay, y2, run.idx, run.w, run.out, run.ws, s)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert run.status() == ep.EP_OK
+    assert_layout_equal(run.layout_np(), eager.layout_np(), wl.expand)
+    assert torch.equal(run.recv.recv_x.view(torch.uint8), eager.recv.recv_x.view(torch.uint8))
+    assert torch.equal(run.out.view(torch.int16), eager.out.view(torch.int16))
