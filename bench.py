@@ -16,6 +16,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -50,11 +51,15 @@ def parse():
     p.add_argument("--zero-padding", action="store_true", help="zero the alignment padding rows")
     p.add_argument("--sf-pack", action="store_true",
                    help="packed power-of-two FP8 scales (4 exponent bytes per word)")
+    p.add_argument("--precast", action="store_true",
+                   help="x arrives already cast to fp8-e4m3 with its scales (FP8 receive only)")
     p.add_argument("--cached", action="store_true",
                    help="time dispatch + combine only, replaying a layout computed once")
     p.add_argument("--compare-sort", action="store_true",
                    help="time the deterministic dispatch against atomic slots + post-hoc sort")
     p.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
+    p.add_argument("--no-ceiling", action="store_true",
+                   help="skip the one-read, many-write copy timed at the dispatch's byte counts")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline sample")
@@ -73,7 +78,26 @@ def workload(args):
         wl = wl.replace(zero_padding=True)
     if args.sf_pack:
         wl = wl.replace(sf_pack=True)
+    if args.precast:
+        if wl.recv_dtype != "fp8":
+            raise SystemExit("--precast needs a workload with an FP8 receive buffer")
+        wl = wl.replace(x_dtype="fp8")
     return wl
+
+
+def host_cpu() -> str:
+    """CPU model and logical core count of this host, for the CPU-baseline line."""
+    model = platform.processor() or platform.machine()
+    try:
+        for line in open("/proc/cpuinfo"):
+            key = line.split(":")[0].strip().lower()
+            if key in ("model name", "cpu part"):
+                val = line.split(":", 1)[1].strip()
+                model = val if key == "model name" else f"{platform.machine()}, CPU part {val}"
+                break
+    except OSError:
+        pass
+    return f"{model}, {os.cpu_count()} logical cores"
 
 
 def describe(wl) -> str:
@@ -123,10 +147,12 @@ def algorithmic_bytes(wl, ntpr, valid_lanes, tokens_with_lane, pad_rows=0):
                 + pad_rows * (H * eb_out + (SW if wl.recv_dtype == "fp8" else 0))  # zeroed padding
                 + ntpr * (K * 8 + K * 4 + (2 + K) * 4)             # sidecar rows
                 + n_tok * K * (8 + 4 + 4))                         # topk_idx, weights, slots read
+    dispatch_read = (tokens_with_lane * H * eb_in + (tokens_with_lane * SW if wl.x_dtype == "fp8" else 0)
+                     + n_tok * K * (8 + 4 + 4))
     combine = (hid_rows * H * 2                                    # each expert-output row once
                + n_tok * H * 2                                     # out written
                + n_tok * K * (8 + 4 + 4))
-    return {"layout": layout, "dispatch": dispatch, "combine": combine}
+    return {"layout": layout, "dispatch": dispatch, "combine": combine, "dispatch_read": dispatch_read}
 
 
 # ---- clocks ----------------------------------------------------------------
@@ -292,9 +318,13 @@ def native(args):
     pad_rows = (int(lay.exp_region[-1].item()) - valid_lanes) if (wl.expand and wl.zero_padding) else 0
     abytes = algorithmic_bytes(wl, ntpr, valid_lanes, tokens_with_lane, pad_rows)
     peak, peak_kind = peaks()
-    gbs = {k: abytes[k] / (phase_ms[k] * 1e-3) / 1e9 for k in abytes}
+    gbs = {k: abytes[k] / (phase_ms[k] * 1e-3) / 1e9 for k in phase_ms}
     dominant = max(("dispatch", "combine"), key=lambda k: phase_ms[k])
 
+    ceiling = None
+    if not args.no_ceiling:
+        ceiling = fanout_ceiling(ep, wl, abytes["dispatch_read"], abytes["dispatch"] - abytes["dispatch_read"],
+                                 gbs["dispatch"], dev, stream, args)
     graph = None
     if not args.no_graph and not args.cached:
         graph = graph_replay(ep, cfg, idx, lay, ws, x, sf, w, recv, y, out, stream, dev, args, world, R * T)
@@ -336,6 +366,8 @@ def native(args):
         line["e2e"] = e2e
     if graph is not None:
         line["graph"] = graph
+    if ceiling is not None:
+        line["dispatch_ceiling"] = ceiling
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, idx_h, w_h, x_h, sf_h, y, args.cpu_seconds)
     if rank == 0:
@@ -343,6 +375,35 @@ def native(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def fanout_ceiling(ep, wl, read_b, write_b, dispatch_gbs, dev, stream, args):
+    """Time the diagnostic fan-out copy (each row read once, written to a run of
+    consecutive rows) moving the dispatch's read and write bytes: both streams
+    sequential, so its rate is the ceiling of a one-read, many-write pass."""
+    row_bytes = wl.hidden * (1 if wl.x_dtype == "fp8" else 2)
+    rows = max(1, round(read_b / row_bytes))
+    den = 1024
+    num = max(1, round(write_b / max(read_b, 1) * den))
+    n_dst = rows * num // den
+    gen = torch.Generator(device=dev).manual_seed(1)
+    src = torch.randint(0, 256, (rows * row_bytes,), dtype=torch.uint8, device=dev, generator=gen)
+    dst = torch.empty(n_dst * row_bytes, dtype=torch.uint8, device=dev)
+    for _ in range(max(args.warmup, 3)):
+        ep.ep_diag_copy_fanout(src, dst, rows, row_bytes, num, den, 0, stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(args.steps):
+        ep.ep_diag_copy_fanout(src, dst, rows, row_bytes, num, den, 0, stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    us = e0.elapsed_time(e1) * 1e3 / args.steps
+    moved = rows * row_bytes + n_dst * row_bytes
+    gbs = moved / (us * 1e-6) / 1e9
+    del src, dst
+    return {"kernel": "fanout_copy_kernel", "read_bytes": rows * row_bytes, "write_bytes": n_dst * row_bytes,
+            "us": us, "gbs": gbs, "dispatch_frac_of_ceiling": dispatch_gbs / gbs}
 
 
 def graph_replay(ep, cfg, idx, lay, ws, x, sf, w, recv, y, out, stream, dev, args, world, units):
@@ -509,7 +570,7 @@ def cpu_baseline(wl, idx_h, w_h, x_h, sf_h, y_dev, seconds):
     per, n, *_ = cpu_sample(wl, idx_h, w_h, x_h, sf_h, y_dev, 64, seed=1)
     n = int(max(64, min(wl.num_ranks * wl.num_tokens, seconds / per)))
     per, n, tl, td, tc = cpu_sample(wl, idx_h, w_h, x_h, sf_h, y_dev, n)
-    return {"value": 1.0 / per, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+    return {"value": 1.0 / per, "unit": "tokens/s", "cores": 1, "kind": "oracle", "host": host_cpu(),
             "sample": (f"full layout of {wl.num_ranks * wl.num_tokens} tokens ({tl:.2f} s) + dispatch "
                        f"and combine of {n} seeded random source tokens ({td:.1f} s + {tc:.1f} s), "
                        f"single-threaded C++ oracle, scaled to tokens/s")}

@@ -21,14 +21,15 @@ import torch
 from . import _build
 
 EP_OK, EP_ERR_INVALID_ARG, EP_ERR_UNSUPPORTED, EP_ERR_WORKSPACE, EP_ERR_CUDA, EP_ERR_BAD_TOPK, \
-    EP_ERR_OVERFLOW = 0, -1, -2, -3, -4, -5, -6
+    EP_ERR_OVERFLOW, EP_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5, -6, -7
 EP_DTYPE_BF16, EP_DTYPE_FP8_E4M3 = 0, 1
 
 __all__ = [
     "Config", "Layout", "Recv", "EpError", "lib", "ep_workspace_bytes", "ep_recv_rows",
     "ep_workspace_init", "ep_get_dispatch_layout", "ep_get_dispatch_layout_noalloc", "ep_dispatch", "ep_combine", "ep_check_error",
     "ep_dispatch_atomic", "ep_deterministic_sort",
-    "ep_status_string", "ep_diag_e4m3_of_bits", "ep_diag_bf16_of_bits", "alloc_layout", "alloc_recv",
+    "ep_status_string", "ep_diag_e4m3_of_bits", "ep_diag_bf16_of_bits",
+    "ep_diag_copy_fanout", "alloc_layout", "alloc_recv",
     "alloc_workspace", "config_of",
 ]
 
@@ -136,6 +137,8 @@ def lib():
         L.ep_diag_e4m3_of_bits.argtypes = [C.c_uint32, C.c_int64, P, P]
         L.ep_diag_bf16_of_bits.restype = I
         L.ep_diag_bf16_of_bits.argtypes = [C.c_uint32, C.c_int64, P, P]
+        L.ep_diag_copy_fanout.restype = I
+        L.ep_diag_copy_fanout.argtypes = [P, P, C.c_int64, I, I, I, I, P]
         _lib = L
     return _lib
 
@@ -302,3 +305,13 @@ def ep_diag_e4m3_of_bits(first: int, out: torch.Tensor, stream=None):
 def ep_diag_bf16_of_bits(first: int, out: torch.Tensor, stream=None):
     _check(lib().ep_diag_bf16_of_bits(first, out.numel(), _ptr(out), _stream(stream)),
            "ep_diag_bf16_of_bits")
+
+
+def ep_diag_copy_fanout(src: torch.Tensor, dst: torch.Tensor, rows: int, row_bytes: int, fan_num: int,
+                        fan_den: int, num_sms: int = 0, stream=None):
+    """Row r of src goes to dst rows floor(r*num/den) .. floor((r+1)*num/den)-1."""
+    need = rows * fan_num // fan_den * row_bytes if fan_den > 0 else 0
+    if src.numel() * src.element_size() < rows * row_bytes or dst.numel() * dst.element_size() < need:
+        raise EpError(EP_ERR_INVALID_ARG, "ep_diag_copy_fanout")
+    _check(lib().ep_diag_copy_fanout(_ptr(src), _ptr(dst), rows, row_bytes, fan_num, fan_den, num_sms,
+                                     _stream(stream)), "ep_diag_copy_fanout")

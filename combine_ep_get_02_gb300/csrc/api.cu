@@ -257,6 +257,7 @@ int ep_dispatch(const ep_config_t* cfg, const ep_layout_t* layout, const void* x
   a.recv_idx = recv->recv_topk_idx;
   a.recv_w = recv->recv_topk_weights;
   a.recv_md = recv->recv_src_metadata;
+  a.err = at<uint32_t>(workspace, workspace_layout(g).err);
   a.R = g.R;
   a.E = g.E;
   a.L = g.L;
@@ -421,6 +422,7 @@ int ep_check_error(void* workspace, void* stream) {
   }
   if (bits & kErrBadTopk) return EP_ERR_BAD_TOPK;
   if (bits & kErrOverflow) return EP_ERR_OVERFLOW;
+  if (bits & kErrTimeout) return EP_ERR_TIMEOUT;
   return EP_OK;
 }
 
@@ -433,6 +435,7 @@ const char* ep_status_string(int status) {
     case EP_ERR_CUDA: return "EP_ERR_CUDA";
     case EP_ERR_BAD_TOPK: return "EP_ERR_BAD_TOPK";
     case EP_ERR_OVERFLOW: return "EP_ERR_OVERFLOW";
+    case EP_ERR_TIMEOUT: return "EP_ERR_TIMEOUT";
     default: return "EP_ERR_UNKNOWN";
   }
 }

@@ -157,8 +157,7 @@ cudaError_t launch_dispatch(const Geometry& g, const DispatchArgs& a, int num_sm
     return g.expand ? launch_one<kCastRow, true>(a, num_sms, stream)
                     : launch_one<kCastRow, false>(a, num_sms, stream);
   }
-  return g.expand ? launch_one<kCopyRow, true>(a, num_sms, stream)
-                  : launch_one<kCopyRow, false>(a, num_sms, stream);
+  return launch_dispatch_bulk(g, a, num_sms, stream);
 }
 
 cudaError_t launch_dispatch_atomic(const Geometry& g, const DispatchArgs& a, int num_sms,

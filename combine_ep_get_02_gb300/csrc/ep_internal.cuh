@@ -15,12 +15,15 @@ constexpr int kMaxTopk = 32;
 constexpr int kMaxExperts = 4096;
 constexpr int kMaxScaleGroups = 128;  // FP8 receive: hidden <= 128 * 128
 constexpr int kCopyThreads = 256;     // dispatch / combine CTA size (8 warps)
+constexpr int kBulkThreads = 128;     // bulk-copy dispatch CTA size (4 warps)
+constexpr int kBulkStageMax = 16384;  // bytes of one shared-memory stage of the bulk-copy dispatch
 constexpr int kMaxPrologueCtas = 64;
 constexpr int kMaxSortRows = 8192;   // rows of one segment the comparison sort handles
 
 // device error bits latched in the workspace header
 constexpr uint32_t kErrBadTopk = 1u;
 constexpr uint32_t kErrOverflow = 2u;
+constexpr uint32_t kErrTimeout = 4u;  // a bounded wait on a copy gave up
 
 // Sizes derived from an ep_config_t that passed validation.
 struct Geometry {
@@ -81,6 +84,7 @@ struct DispatchArgs {
   int64_t* recv_idx;
   float* recv_w;
   int32_t* recv_md;
+  uint32_t* err;             // the workspace's device error bits
   int R, E, L, K, T, H, G, M, compact, zero_padding, n_so, n_su, sf_pack;
   int SW;  // 32-bit words of one row's scale sidecar
   int64_t region_rows;
@@ -125,6 +129,10 @@ struct CombineArgs {
 
 cudaError_t launch_layout(const Geometry& g, const LayoutArgs& a, int num_prologue_sms,
                           cudaStream_t stream);
+// Rows that travel unchanged, through shared memory with bulk copies
+// (dispatch_bulk.cu); the stage size a row of row_bytes is split into.
+cudaError_t launch_dispatch_bulk(const Geometry& g, const DispatchArgs& a, int num_sms, cudaStream_t stream);
+int dispatch_bulk_stage_bytes(int row_bytes);
 cudaError_t launch_dispatch(const Geometry& g, const DispatchArgs& a, int num_sms,
                             cudaStream_t stream);
 cudaError_t launch_dispatch_atomic(const Geometry& g, const DispatchArgs& a, int num_sms,

@@ -49,6 +49,9 @@ extern "C" {
                                    or a repeated expert in the expanded layout */
 #define EP_ERR_OVERFLOW (-6)    /* a row would not fit (cannot happen when
                                    num_tokens <= num_max_tokens_per_rank)   */
+#define EP_ERR_TIMEOUT (-7)     /* device: a bounded wait for a bulk copy gave
+                                   up (the kernel returned early; its
+                                   outputs are incomplete)                   */
 
 /* ---- element types ------------------------------------------------------- */
 #define EP_DTYPE_BF16 0
@@ -256,6 +259,19 @@ const char* ep_status_string(int status);
  * memory of n bytes / n uint16. */
 int ep_diag_e4m3_of_bits(uint32_t first, int64_t n, uint8_t* out, void* stream);
 int ep_diag_bf16_of_bits(uint32_t first, int64_t n, uint16_t* out, void* stream);
+
+/* Diagnostic copy for the bandwidth ceiling of a one-read, many-write stream
+ * (no counterpart on the pages; the benchmark times it beside the dispatch,
+ * whose scatter reads each token row once and writes it to each destination).
+ * Row r of `src` (device, rows x row_bytes, 16-byte aligned) is read once and
+ * written to rows floor(r*fan_num/fan_den) .. floor((r+1)*fan_num/fan_den) - 1
+ * of `dst` (device, 16-byte aligned, floor(rows*fan_num/fan_den) rows of
+ * row_bytes; the caller owns both). row_bytes: a positive multiple of 16;
+ * 0 <= fan_num <= 2^20, fan_den >= 1, 0 <= rows <= 2^40; num_sms: SMs the grid
+ * is sized for (0 = all). Returns EP_ERR_INVALID_ARG for any other argument,
+ * EP_ERR_CUDA if the launch fails; asynchronous on `stream`. */
+int ep_diag_copy_fanout(const void* src, void* dst, int64_t rows, int32_t row_bytes, int32_t fan_num,
+                        int32_t fan_den, int32_t num_sms, void* stream);
 
 #ifdef __cplusplus
 }

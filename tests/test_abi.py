@@ -134,6 +134,20 @@ def test_misaligned_rows_are_rejected(ep):
     assert st == ep.EP_ERR_INVALID_ARG
 
 
+def test_diag_copy_rejects_bad_arguments(ep):
+    L, P = ep.lib(), C.c_void_p
+    a, b = P(0x100000), P(0x200000)
+    for rows, rb, num, den, sms in ((1, 24, 1, 1, 0), (1, 0, 1, 1, 0), (1, 16, 1, 0, 0), (-1, 16, 1, 1, 0),
+                                    (1, 16, -1, 1, 0), (1, 16, (1 << 20) + 1, 1, 0), (1 << 41, 16, 1, 1, 0),
+                                    (1, 16, 1, 1, -1)):
+        assert L.ep_diag_copy_fanout(a, b, rows, rb, num, den, sms, None) == ep.EP_ERR_INVALID_ARG
+    assert L.ep_diag_copy_fanout(P(0x100008), b, 1, 16, 1, 1, 0, None) == ep.EP_ERR_INVALID_ARG
+    assert L.ep_diag_copy_fanout(a, None, 1, 16, 1, 1, 0, None) == ep.EP_ERR_INVALID_ARG
+    # nothing to copy: accepted without a launch
+    assert L.ep_diag_copy_fanout(None, None, 0, 16, 3, 1, 0, None) == ep.EP_OK
+    assert L.ep_diag_copy_fanout(None, None, 5, 16, 0, 1, 0, None) == ep.EP_OK
+
+
 def test_status_strings(ep):
     assert ep.ep_status_string(0) == "EP_OK"
     assert ep.ep_status_string(-5) == "EP_ERR_BAD_TOPK"

@@ -37,6 +37,11 @@ EXTRA = {
     "odd_r6": W.Workload("odd_r6", 3, 2, 18, 3, 33, 40, 8, mask_frac=0.2),
     # one token per rank
     "one_token": W.Workload("one_token", 1, 16, 256, 8, 1, 4, 7168, y_kind="random"),
+    # bf16 rows wider than one shared-memory stage of the bulk-copy dispatch (two pieces, the
+    # second shorter), row form and expanded with zeroed padding
+    "wide_rows": W.Workload("wide_rows", 1, 8, 64, 6, 150, 160, 12296, mask_frac=0.1),
+    "wide_expand": W.Workload("wide_expand", 1, 4, 16, 4, 70, 70, 8200, expand=True,
+                              expert_alignment=4, zero_padding=True, y_kind="random"),
 }
 
 CASES = dict(W.PARITY)
