@@ -44,7 +44,7 @@ class _Config(C.Structure):
     _fields_ = [(n, C.c_int32) for n in (
         "num_scaleout_ranks", "num_scaleup_ranks", "num_experts", "num_topk", "num_tokens",
         "num_max_tokens_per_rank", "hidden", "x_dtype", "recv_dtype", "expand", "expert_alignment",
-        "num_sms", "num_prologue_sms", "compact_recv", "zero_padding", "sf_pack")]
+        "num_sms", "num_prologue_sms", "compact_recv", "zero_padding", "sf_pack", "copy_path")]
 
 
 class _Layout(C.Structure):
@@ -77,6 +77,7 @@ class Config:
     compact_recv: int = 0
     zero_padding: int = 0
     sf_pack: int = 0
+    copy_path: int = 0  # unchanged rows: 0 automatic, 1 register copies, 2 bulk copies
 
     @property
     def num_ranks(self) -> int:
@@ -138,7 +139,7 @@ def lib():
         L.ep_diag_bf16_of_bits.restype = I
         L.ep_diag_bf16_of_bits.argtypes = [C.c_uint32, C.c_int64, P, P]
         L.ep_diag_copy_fanout.restype = I
-        L.ep_diag_copy_fanout.argtypes = [P, P, C.c_int64, I, I, I, I, P]
+        L.ep_diag_copy_fanout.argtypes = [P, P, C.c_int64, I, I, I, I, I, P]
         _lib = L
     return _lib
 
@@ -308,10 +309,11 @@ def ep_diag_bf16_of_bits(first: int, out: torch.Tensor, stream=None):
 
 
 def ep_diag_copy_fanout(src: torch.Tensor, dst: torch.Tensor, rows: int, row_bytes: int, fan_num: int,
-                        fan_den: int, num_sms: int = 0, stream=None):
-    """Row r of src goes to dst rows floor(r*num/den) .. floor((r+1)*num/den)-1."""
+                        fan_den: int, num_sms: int = 0, method: int = 0, stream=None):
+    """Row r of src goes to dst rows floor(r*num/den) .. floor((r+1)*num/den)-1;
+    method 0: register loads/stores, 1: bulk copies through shared memory."""
     need = rows * fan_num // fan_den * row_bytes if fan_den > 0 else 0
     if src.numel() * src.element_size() < rows * row_bytes or dst.numel() * dst.element_size() < need:
         raise EpError(EP_ERR_INVALID_ARG, "ep_diag_copy_fanout")
     _check(lib().ep_diag_copy_fanout(_ptr(src), _ptr(dst), rows, row_bytes, fan_num, fan_den, num_sms,
-                                     _stream(stream)), "ep_diag_copy_fanout")
+                                     method, _stream(stream)), "ep_diag_copy_fanout")

@@ -78,6 +78,7 @@ int make_geometry(const ep_config_t* c, Geometry* g) {
   if (c->zero_padding && !c->expand) return EP_ERR_UNSUPPORTED;  // only expanded blocks are padded
   if (c->sf_pack != 0 && c->sf_pack != 1) return EP_ERR_INVALID_ARG;
   if (c->sf_pack && c->recv_dtype != EP_DTYPE_FP8_E4M3) return EP_ERR_UNSUPPORTED;
+  if (c->copy_path < 0 || c->copy_path > 2) return EP_ERR_INVALID_ARG;
   // 32-bit row indices: rows of one region, lanes, and expanded rows must fit
   const int64_t region_rows = R * c->num_max_tokens_per_rank;
   const int64_t lanes = R * c->num_tokens * c->num_topk;
@@ -101,6 +102,7 @@ int make_geometry(const ep_config_t* c, Geometry* g) {
   g->compact = c->compact_recv;
   g->zero_padding = c->zero_padding;
   g->sf_pack = c->sf_pack;
+  g->copy_path = c->copy_path;
   g->SW = c->sf_pack ? (g->G + 3) / 4 : g->G;
   g->region_rows = region_rows;
   g->num_tokens = R * c->num_tokens;

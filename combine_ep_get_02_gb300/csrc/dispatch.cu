@@ -157,7 +157,13 @@ cudaError_t launch_dispatch(const Geometry& g, const DispatchArgs& a, int num_sm
     return g.expand ? launch_one<kCastRow, true>(a, num_sms, stream)
                     : launch_one<kCastRow, false>(a, num_sms, stream);
   }
-  return launch_dispatch_bulk(g, a, num_sms, stream);
+  // Unchanged rows: bulk copies pay off once the input streams from DRAM; on small
+  // (L2-resident, latency-bound) inputs the register path has more rows in flight.
+  const bool bulk = g.copy_path == 2 ||
+                    (g.copy_path == 0 && a.num_tokens * a.in_row_bytes >= kBulkAutoMinBytes);
+  if (bulk) return launch_dispatch_bulk(g, a, num_sms, stream);
+  return g.expand ? launch_one<kCopyRow, true>(a, num_sms, stream)
+                  : launch_one<kCopyRow, false>(a, num_sms, stream);
 }
 
 cudaError_t launch_dispatch_atomic(const Geometry& g, const DispatchArgs& a, int num_sms,

@@ -21,57 +21,10 @@ namespace {
 
 constexpr int kBulkWarps = kBulkThreads / 32;
 constexpr int kBulkStages = 2;
-constexpr uint32_t kBulkWaitLimit = 1u << 24;  // try_wait rounds before giving up
 // One CTA (four warps, four rows in flight) per SM: on GB300 more concurrent
 // row streams measured slower (2-6% on 4K-14K-byte rows), not faster.
 constexpr int kBulkMaxCtasPerSm = 1;
 static_assert(kBulkThreads / 32 * 2 * kBulkStageMax <= 160 * 1024, "bulk stages exceed shared memory");
-
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
-}
-
-// global -> shared bulk copy of `bytes` (multiple of 16), counted on `bar`
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
-// shared -> global bulk copy, tracked by the issuing thread's bulk groups
-__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-
-// every committed store has finished reading shared memory
-__device__ __forceinline__ void bulk_wait_reads() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
-// bounded wait for the phase of `bar` with parity `parity` to complete
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kBulkWaitLimit; ++i) {
-    uint32_t done;
-    asm volatile(
-        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
-        : "=r"(done)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    if (done) return true;
-  }
-  return false;
-}
 
 template <bool kExpand>
 __global__ void __launch_bounds__(kBulkThreads) dispatch_bulk_kernel(DispatchArgs a, int stage_bytes) {
@@ -138,7 +91,7 @@ __global__ void __launch_bounds__(kBulkThreads) dispatch_bulk_kernel(DispatchArg
       if (ntok < a.num_tokens) load_piece(ntok, last ? 0 : piece + 1, stage ^ 1);
       // store this piece to every destination row once it has landed
       int landed = 1;
-      if (lane == 0) landed = mbar_wait(bar_addr(stage), (parity >> stage) & 1u);
+      if (lane == 0) landed = mbar_wait(bar_addr(stage), (parity >> stage) & 1u, kBulkWaitLimit);
       landed = __shfl_sync(kFullMask, landed, 0);
       if (!landed) {
         ok = false;
@@ -172,7 +125,7 @@ __global__ void __launch_bounds__(kBulkThreads) dispatch_bulk_kernel(DispatchArg
     // never leave with a load still writing this warp's stages
 #pragma unroll
     for (int s = 0; s < kBulkStages; ++s)
-      if (((pending >> s) & 1u) && !mbar_wait(bar_addr(s), (parity >> s) & 1u)) ok = false;
+      if (((pending >> s) & 1u) && !mbar_wait(bar_addr(s), (parity >> s) & 1u, kBulkWaitLimit)) ok = false;
     bulk_wait_all();
     if (!ok) atomicOr(a.err, kErrTimeout);
   }

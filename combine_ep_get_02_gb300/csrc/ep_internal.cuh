@@ -17,6 +17,7 @@ constexpr int kMaxScaleGroups = 128;  // FP8 receive: hidden <= 128 * 128
 constexpr int kCopyThreads = 256;     // dispatch / combine CTA size (8 warps)
 constexpr int kBulkThreads = 128;     // bulk-copy dispatch CTA size (4 warps)
 constexpr int kBulkStageMax = 16384;  // bytes of one shared-memory stage of the bulk-copy dispatch
+constexpr int64_t kBulkAutoMinBytes = int64_t{32} << 20;  // input rows from which copy_path 0 picks bulk
 constexpr int kMaxPrologueCtas = 64;
 constexpr int kMaxSortRows = 8192;   // rows of one segment the comparison sort handles
 
@@ -29,6 +30,7 @@ constexpr uint32_t kErrTimeout = 4u;  // a bounded wait on a copy gave up
 struct Geometry {
   int R, n_so, n_su, E, L, K, T, M, H, G;
   int x_fp8, recv_fp8, expand, align, compact, zero_padding, sf_pack;
+  int copy_path;  // 0 automatic, 1 register copies, 2 bulk copies (rows that travel unchanged)
   int SW;  // 32-bit words of one row's scale sidecar: G, or ceil(G/4) packed
   int64_t region_rows;  // rows of one destination region in the row form: R * M
   int64_t num_tokens;   // R * T

@@ -98,6 +98,13 @@ typedef struct ep_config {
                                       per 32-bit word, group g in byte g%4 of word g/4,
                                       so a row holds ceil(G/4) words. Pre-cast FP8
                                       input then carries x_sf in the same packing.  */
+  int32_t copy_path;               /* how dispatch moves rows that travel unchanged
+                                      (bf16 -> bf16, pre-cast FP8): 0 = automatic
+                                      (bulk copies when the input rows total
+                                      at least 32 MiB, register copies below);
+                                      1 = 16-byte register loads and stores; 2 = bulk
+                                      copies through shared memory. Results never
+                                      depend on it; the fused cast ignores it.     */
 } ep_config_t;
 
 /* ---- dispatch layout (all device pointers, int32 unless noted) -------------
@@ -268,10 +275,12 @@ int ep_diag_bf16_of_bits(uint32_t first, int64_t n, uint16_t* out, void* stream)
  * of `dst` (device, 16-byte aligned, floor(rows*fan_num/fan_den) rows of
  * row_bytes; the caller owns both). row_bytes: a positive multiple of 16;
  * 0 <= fan_num <= 2^20, fan_den >= 1, 0 <= rows <= 2^40; num_sms: SMs the grid
- * is sized for (0 = all). Returns EP_ERR_INVALID_ARG for any other argument,
+ * is sized for (0 = all). method 0: 16-byte register loads and stores; method
+ * 1: bulk copies through shared memory (row_bytes <= 16384, else
+ * EP_ERR_UNSUPPORTED). Returns EP_ERR_INVALID_ARG for any other argument,
  * EP_ERR_CUDA if the launch fails; asynchronous on `stream`. */
 int ep_diag_copy_fanout(const void* src, void* dst, int64_t rows, int32_t row_bytes, int32_t fan_num,
-                        int32_t fan_den, int32_t num_sms, void* stream);
+                        int32_t fan_den, int32_t num_sms, int32_t method, void* stream);
 
 #ifdef __cplusplus
 }

@@ -86,6 +86,8 @@ def test_workspace_bytes_closed_form(ep):
     (dict(zero_padding=3, expand=1), -1),
     (dict(sf_pack=1), -2),                    # packed scales need an FP8 receive
     (dict(sf_pack=2, recv_dtype=1), -1),
+    (dict(copy_path=3), -1),
+    (dict(copy_path=-1), -1),
 ])
 def test_invalid_configs_are_rejected_before_any_launch(ep, bad, code):
     c = cfg(ep, **bad)
@@ -140,17 +142,21 @@ def test_diag_copy_rejects_bad_arguments(ep):
     for rows, rb, num, den, sms in ((1, 24, 1, 1, 0), (1, 0, 1, 1, 0), (1, 16, 1, 0, 0), (-1, 16, 1, 1, 0),
                                     (1, 16, -1, 1, 0), (1, 16, (1 << 20) + 1, 1, 0), (1 << 41, 16, 1, 1, 0),
                                     (1, 16, 1, 1, -1)):
-        assert L.ep_diag_copy_fanout(a, b, rows, rb, num, den, sms, None) == ep.EP_ERR_INVALID_ARG
-    assert L.ep_diag_copy_fanout(P(0x100008), b, 1, 16, 1, 1, 0, None) == ep.EP_ERR_INVALID_ARG
-    assert L.ep_diag_copy_fanout(a, None, 1, 16, 1, 1, 0, None) == ep.EP_ERR_INVALID_ARG
+        assert L.ep_diag_copy_fanout(a, b, rows, rb, num, den, sms, 0, None) == ep.EP_ERR_INVALID_ARG
+    assert L.ep_diag_copy_fanout(P(0x100008), b, 1, 16, 1, 1, 0, 0, None) == ep.EP_ERR_INVALID_ARG
+    assert L.ep_diag_copy_fanout(a, None, 1, 16, 1, 1, 0, 0, None) == ep.EP_ERR_INVALID_ARG
+    assert L.ep_diag_copy_fanout(a, b, 1, 16, 1, 1, 0, 2, None) == ep.EP_ERR_INVALID_ARG
+    # rows wider than one shared-memory stage: no bulk method
+    assert L.ep_diag_copy_fanout(a, b, 1, 16400, 1, 1, 0, 1, None) == ep.EP_ERR_UNSUPPORTED
     # nothing to copy: accepted without a launch
-    assert L.ep_diag_copy_fanout(None, None, 0, 16, 3, 1, 0, None) == ep.EP_OK
-    assert L.ep_diag_copy_fanout(None, None, 5, 16, 0, 1, 0, None) == ep.EP_OK
+    assert L.ep_diag_copy_fanout(None, None, 0, 16, 3, 1, 0, 0, None) == ep.EP_OK
+    assert L.ep_diag_copy_fanout(None, None, 5, 16, 0, 1, 0, 1, None) == ep.EP_OK
 
 
 def test_status_strings(ep):
     assert ep.ep_status_string(0) == "EP_OK"
     assert ep.ep_status_string(-5) == "EP_ERR_BAD_TOPK"
+    assert ep.ep_status_string(-7) == "EP_ERR_TIMEOUT"
     assert ep.ep_status_string(-99) == "EP_ERR_UNKNOWN"
 
 

@@ -5,7 +5,8 @@ Every assignment of {-1, 0..E-1} to one source's 3 tokens x 2 lanes (E = 4:
 and through the oracle. One call carries R routings, one per source rank, so
 ceil(15,625 / R) calls cover the enumeration; the layouts, every receive row,
 the sidecars of the filled rows and the combined tokens must match bit for
-bit. Expanded layouts enumerate the routings without an expert repeated inside
+bit, with unchanged rows moved both by register copies and by bulk copies.
+Expanded layouts enumerate the routings without an expert repeated inside
 a token (21^3 = 9,261), a repeat being an error there.
 
 The oracle itself is pinned on the same enumeration against the sort-based
@@ -58,8 +59,11 @@ def test_enumeration_sizes():
     assert routings(True).shape == (9261, T, K)
 
 
-@pytest.mark.parametrize("name", list(SHAPES))
-def test_every_routing_matches_the_oracle(name):
+CASES = [(name, path) for name in SHAPES for path in ((0,) if SHAPES[name].recv_dtype == "fp8" else (1, 2))]
+
+
+@pytest.mark.parametrize("name,copy_path", CASES)
+def test_every_routing_matches_the_oracle(name, copy_path):
     wl = SHAPES[name]
     R, M, H = wl.num_ranks, wl.num_max_tokens_per_rank, wl.hidden
     cases = routings(wl.expand)
@@ -67,7 +71,7 @@ def test_every_routing_matches_the_oracle(name):
     # wrap around so the last call is full; every routing appears at least once
     order = np.arange(n_calls * R) % len(cases)
 
-    cfg = ep.config_of(wl)
+    cfg = ep.config_of(wl, copy_path=copy_path)
     dev = "cuda"
     _, w = W.routing(wl)                 # fp32 weights [R, T, K]; masked lanes are skipped
     x, sf = W.hidden(wl)

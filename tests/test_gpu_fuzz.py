@@ -2,8 +2,8 @@
 
 Each case draws a small configuration (ranks, scale-out split, experts per rank,
 top-k, tokens, max tokens, hidden, input/receive dtypes, expanded or row form,
-alignment and zero padding, compact rows, packed scales, masking) from a seeded
-generator, runs layout -> dispatch -> combine through the C ABI and compares
+alignment and zero padding, compact rows, packed scales, masking, the way unchanged
+rows are copied) from a seeded generator, runs layout -> dispatch -> combine through the C ABI and compares
 every output with the oracle: layouts, every row of the receive buffers (which
 start filled with 0xFF, so untouched rows must stay 0xFF and padding rows must
 become zero), the scale and sidecar rows, and the combined tokens.
@@ -57,7 +57,8 @@ def test_fuzz_case(seed):
     idx, w, x, sf = inputs(wl)
     st, olay = oracle.layout(wl, idx)
     assert st == 0
-    run = GpuRun(wl, idx, w, x, sf, num_prologue_sms=seed % 5 * 7, num_sms=(seed % 3) * 11).layout()
+    run = GpuRun(wl, idx, w, x, sf, num_prologue_sms=seed % 5 * 7, num_sms=(seed % 3) * 11,
+                 copy_path=seed % 3).layout()
     run.recv = ep.alloc_recv(run.cfg, run.dev)
     for t in (run.recv.recv_x, run.recv.recv_sf, run.recv.recv_topk_idx, run.recv.recv_topk_weights,
               run.recv.recv_src_metadata):

@@ -64,9 +64,12 @@ def test_layout(case):
     assert_layout_equal(run.layout_np(), olay, wl.expand)
 
 
-def test_dispatch(case):
+@pytest.mark.parametrize("copy_path", [1, 2])
+def test_dispatch(case, copy_path):
+    """Both ways of moving unchanged rows (register copies, bulk copies through
+    shared memory); the fused cast ignores the setting."""
     wl, idx, w, x, sf, olay = case
-    run = GpuRun(wl, idx, w, x, sf).layout().dispatch()
+    run = GpuRun(wl, idx, w, x, sf, copy_path=copy_path).layout().dispatch()
     assert run.status() == ep.EP_OK
     st, orec = oracle.dispatch(wl, olay, x, sf, idx, w)
     assert st == 0
