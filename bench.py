@@ -519,14 +519,15 @@ def end_to_end(ep, cfg, wl, idx_h, w_h, x_h, sf_h, lay, recv, y, identity, ws, s
 
 def ncu_traffic(kernel, wl, n_tok):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, if it was
-    taken on the current kernel source; scaled by source tokens when the capture
-    ran a smaller case. None when there is no matching capture."""
+    taken on the kernel's current sources (its unit and the headers it includes);
+    scaled by source tokens when the capture ran a smaller case. None when there
+    is no matching capture."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(path):
         return None
     try:
         from combine_ep_get_02_gb300 import _build
-        src = _build.source_hash()
+        src = _build.source_hash(kernel)
         for line in open(path):
             f = line.split()
             if len(f) == 6 and f[0] == kernel and f[1] == wl.name and f[5] == src:

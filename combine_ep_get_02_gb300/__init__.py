@@ -29,7 +29,7 @@ __all__ = [
     "ep_workspace_init", "ep_get_dispatch_layout", "ep_get_dispatch_layout_noalloc", "ep_dispatch", "ep_combine", "ep_check_error",
     "ep_dispatch_atomic", "ep_deterministic_sort",
     "ep_status_string", "ep_diag_e4m3_of_bits", "ep_diag_bf16_of_bits",
-    "ep_diag_copy_fanout", "alloc_layout", "alloc_recv",
+    "ep_diag_copy_fanout", "ep_diag_wait_timeout", "alloc_layout", "alloc_recv",
     "alloc_workspace", "config_of",
 ]
 
@@ -140,6 +140,8 @@ def lib():
         L.ep_diag_bf16_of_bits.argtypes = [C.c_uint32, C.c_int64, P, P]
         L.ep_diag_copy_fanout.restype = I
         L.ep_diag_copy_fanout.argtypes = [P, P, C.c_int64, I, I, I, I, I, P]
+        L.ep_diag_wait_timeout.restype = I
+        L.ep_diag_wait_timeout.argtypes = [P, P, I, C.c_uint32, P]
         _lib = L
     return _lib
 
@@ -317,3 +319,10 @@ def ep_diag_copy_fanout(src: torch.Tensor, dst: torch.Tensor, rows: int, row_byt
         raise EpError(EP_ERR_INVALID_ARG, "ep_diag_copy_fanout")
     _check(lib().ep_diag_copy_fanout(_ptr(src), _ptr(dst), rows, row_bytes, fan_num, fan_den, num_sms,
                                      method, _stream(stream)), "ep_diag_copy_fanout")
+
+
+def ep_diag_wait_timeout(ws: torch.Tensor, src, nbytes: int, rounds: int, stream=None):
+    """Run the bulk-copy dispatch's abort sequence: a wait that runs out after
+    `rounds` rounds with a load of `nbytes` from `src` in flight."""
+    _check(lib().ep_diag_wait_timeout(_ptr(ws), _ptr(src), nbytes, rounds,
+                                      _stream(stream)), "ep_diag_wait_timeout")

@@ -37,14 +37,36 @@ def _deps():
     return sources() + hdr + [os.path.abspath(__file__)]
 
 
-def source_hash() -> str:
-    """Short hash of every kernel source and header (identifies a build's kernels)."""
+# translation unit that holds each kernel (and its launcher)
+KERNEL_UNITS = {"layout_kernel": "layout.cu", "dispatch_kernel": "dispatch.cu",
+                "dispatch_bulk_kernel": "dispatch_bulk.cu", "combine_kernel": "combine.cu"}
+
+
+def kernel_sources(kernel: str) -> list:
+    """The kernel's translation unit and the library headers it includes, recursively."""
+    import re
+    seen, stack = [], [os.path.join(CSRC, KERNEL_UNITS[kernel])]
+    while stack:
+        p = stack.pop()
+        if p in seen:
+            continue
+        seen.append(p)
+        for name in re.findall(r'#include\s+"([^"]+)"', open(p).read()):
+            q = os.path.join(CSRC, name)
+            if os.path.exists(q):
+                stack.append(q)
+    return sorted(seen)
+
+
+def source_hash(kernel: str = None) -> str:
+    """Short hash of one kernel's sources (its unit and the csrc headers it
+    includes), or of every source and header when no kernel is named."""
     import hashlib
+    files = kernel_sources(kernel) if kernel else [p for p in sorted(_deps()) if p.endswith((".cu", ".cuh", ".h"))]
     h = hashlib.sha256()
-    for p in sorted(_deps()):
-        if p.endswith((".cu", ".cuh", ".h")):
-            h.update(os.path.basename(p).encode())
-            h.update(open(p, "rb").read())
+    for p in files:
+        h.update(os.path.basename(p).encode())
+        h.update(open(p, "rb").read())
     return h.hexdigest()[:16]
 
 

@@ -282,6 +282,15 @@ int ep_diag_bf16_of_bits(uint32_t first, int64_t n, uint16_t* out, void* stream)
 int ep_diag_copy_fanout(const void* src, void* dst, int64_t rows, int32_t row_bytes, int32_t fan_num,
                         int32_t fan_den, int32_t num_sms, int32_t method, void* stream);
 
+/* Diagnostic for the bounded waits (no counterpart on the pages): one warp
+ * starts a bulk load of `bytes` (0..4096, a multiple of 16) from `src` (device,
+ * 16-byte aligned; may be null when bytes is 0), waits at most `rounds`
+ * (<= 2^20) try_wait rounds on an mbarrier that nothing completes, drains the
+ * load and latches the timeout bit in `workspace` (256-byte aligned), exactly
+ * as the bulk-copy dispatch does when a wait runs out; ep_check_error then
+ * returns EP_ERR_TIMEOUT. Asynchronous on `stream`. */
+int ep_diag_wait_timeout(void* workspace, const void* src, int32_t bytes, uint32_t rounds, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

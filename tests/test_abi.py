@@ -153,6 +153,16 @@ def test_diag_copy_rejects_bad_arguments(ep):
     assert L.ep_diag_copy_fanout(None, None, 5, 16, 0, 1, 0, 1, None) == ep.EP_OK
 
 
+def test_diag_wait_timeout_rejects_bad_arguments(ep):
+    L, P = ep.lib(), C.c_void_p
+    ws, src = P(0x100000), P(0x200000)
+    assert L.ep_diag_wait_timeout(None, src, 16, 1, None) == ep.EP_ERR_WORKSPACE
+    assert L.ep_diag_wait_timeout(P(0x100010), src, 16, 1, None) == ep.EP_ERR_WORKSPACE
+    for s, n, r in ((src, 4112, 1), (src, 24, 1), (src, -16, 1), (None, 16, 1), (P(0x200008), 16, 1),
+                    (src, 16, (1 << 20) + 1)):
+        assert L.ep_diag_wait_timeout(ws, s, n, r, None) == ep.EP_ERR_INVALID_ARG
+
+
 def test_status_strings(ep):
     assert ep.ep_status_string(0) == "EP_OK"
     assert ep.ep_status_string(-5) == "EP_ERR_BAD_TOPK"
