@@ -471,7 +471,7 @@ def end_to_end(ep, cfg, wl, idx_h, w_h, x_h, sf_h, lay, recv, y, identity, ws, s
     in_done = [ev() for _ in range(nb)]
     comp_done = [ev() for _ in range(nb)]
     out_done = [ev() for _ in range(nb)]
-    steps = max(3, min(args.steps, 10))
+    steps = max(40, args.steps)  # a job long enough that pipeline fill and drain stay small
 
     def run(n):
         for i in range(n):
@@ -512,9 +512,42 @@ def end_to_end(ep, cfg, wl, idx_h, w_h, x_h, sf_h, lay, recv, y, identity, ws, s
     h2d = hx.numel() * hx.element_size() + hidx.numel() * 8 + hw.numel() * 4 + \
         (0 if hsf is None else hsf.numel() * 4)
     d2h = hout[0].numel() * 2
+
+    link_ms = transfer_only_ms(hx, hidx, hw, hsf, dx[0], didx[0], dw[0], dsf[0], hout[1], dout[1], stream, dev)
     return {"value": whole_job_rate(world, R * T, ms * steps, steps), "unit": "tokens/s",
             "ms_per_step": ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "pipeline": "double-buffered host copies on two copy streams"}
+            "steps": steps, "transfer_only_ms_per_step": link_ms,
+            "pipeline": "double-buffered host copies on two copy streams, overlapped with the kernels"}
+
+
+def transfer_only_ms(hx, hidx, hw, hsf, dx, didx, dw, dsf, hout, dout, stream, dev, reps=5):
+    """One step's input copied in and its output copied back at the same time,
+    with no kernels: the host link's bound on the end-to-end step."""
+    t_in, t_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def once():
+        t_in.wait_stream(stream)
+        t_out.wait_stream(stream)
+        with torch.cuda.stream(t_in):
+            dx.copy_(hx, non_blocking=True)
+            didx.copy_(hidx, non_blocking=True)
+            dw.copy_(hw, non_blocking=True)
+            if dsf is not None:
+                dsf.copy_(hsf, non_blocking=True)
+        with torch.cuda.stream(t_out):
+            hout.copy_(dout, non_blocking=True)
+        stream.wait_stream(t_in)
+        stream.wait_stream(t_out)
+
+    once()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        once()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    return a.elapsed_time(b) / reps
 
 
 def ncu_traffic(kernel, wl, n_tok):

@@ -42,6 +42,18 @@ EXTRA = {
     "wide_rows": W.Workload("wide_rows", 1, 8, 64, 6, 150, 160, 12296, mask_frac=0.1),
     "wide_expand": W.Workload("wide_expand", 1, 4, 16, 4, 70, 70, 8200, expand=True,
                               expert_alignment=4, zero_padding=True, y_kind="random"),
+    # the library's limits: 64 ranks, 4096 experts, top-32; hidden 16384 with FP8 (128 scale
+    # groups, 32 packed scale words)
+    "max_ranks_experts": W.Workload("max_ranks_experts", 1, 64, 4096, 32, 40, 48, 128, mask_frac=0.1,
+                                    routing="zipf"),
+    "max_expand": W.Workload("max_expand", 4, 16, 4096, 32, 30, 30, 256, expand=True, expert_alignment=8,
+                             zero_padding=True, y_kind="random"),
+    "max_hidden_fp8": W.Workload("max_hidden_fp8", 1, 4, 16, 4, 40, 40, 16384, recv_dtype="fp8",
+                                 routing="zipf"),
+    "max_hidden_packed": W.Workload("max_hidden_packed", 2, 2, 16, 4, 40, 40, 16384, recv_dtype="fp8",
+                                    sf_pack=True),
+    "max_hidden_precast_packed": W.Workload("max_hidden_precast_packed", 1, 4, 16, 4, 40, 40, 16384,
+                                            x_dtype="fp8", recv_dtype="fp8", sf_pack=True),
 }
 
 CASES = dict(W.PARITY)
