@@ -46,6 +46,24 @@ __device__ __forceinline__ bool aligned16(const void* p) {
   return (reinterpret_cast<uintptr_t>(p) & 15) == 0;
 }
 
+// 32x32 bit-matrix transpose across a warp: on entry lane i holds row i (bit c
+// of x is M[i][c]); on exit lane c holds column c (bit i is M[i][c]), i.e. what
+// __ballot_sync would return for predicate "bit c of my row" -- for all 32
+// columns with five exchanges instead of 32 ballots. Each step swaps the
+// off-diagonal blocks of every 2j x 2j block: the upper lane keeps its left
+// columns and takes its partner's left columns, the lower lane the right ones.
+__device__ __forceinline__ uint32_t warp_transpose32(uint32_t x, int lane) {
+  constexpr uint32_t kLeft[5] = {0x0000FFFFu, 0x00FF00FFu, 0x0F0F0F0Fu, 0x33333333u, 0x55555555u};
+#pragma unroll
+  for (int step = 0; step < 5; ++step) {
+    const int j = 16 >> step;
+    const uint32_t m = kLeft[step];
+    const uint32_t y = __shfl_xor_sync(kFullMask, x, j);
+    x = (lane & j) ? ((x & ~m) | ((y & ~m) >> j)) : ((x & m) | ((y & m) << j));
+  }
+  return x;
+}
+
 // Row block of source s inside every destination region (R blocks of M rows).
 __device__ __forceinline__ int row_block(int s, int n_so, int n_su) {
   return n_so == 1 ? s : (s % n_su) * n_so + s / n_su;
@@ -147,10 +165,12 @@ __global__ void __launch_bounds__(THREADS) layout_kernel(LayoutArgs a) {
 #pragma unroll
       for (int k = 0; k < KMAX; ++k)
         if (e[k] >= 0) atomicAdd(&cnt_e[e[k]], 1);
-      const uint32_t lo = static_cast<uint32_t>(dmask), hi = static_cast<uint32_t>(dmask >> 32);
-      for (int d = 0; d < R; ++d) {
-        const int n = __popc(__ballot_sync(kFullMask, ((d < 32 ? lo : hi) >> (d & 31)) & 1u));
-        if (lane == 0 && n != 0) atomicAdd(&cnt_d[d], n);
+      // lane d: the warp's tokens that reach destination d (and d + 32)
+      const uint32_t col_lo = warp_transpose32(static_cast<uint32_t>(dmask), lane);
+      if (lane < R && col_lo != 0) atomicAdd(&cnt_d[lane], __popc(col_lo));
+      if (R > 32) {
+        const uint32_t col_hi = warp_transpose32(static_cast<uint32_t>(dmask >> 32), lane);
+        if (lane + 32 < R && col_hi != 0) atomicAdd(&cnt_d[lane + 32], __popc(col_hi));
       }
 #pragma unroll
       for (int k = 0; k < KMAX; ++k) e[k] = en[k];
@@ -204,10 +224,12 @@ __global__ void __launch_bounds__(THREADS) layout_kernel(LayoutArgs a) {
         for (int k = 0; k < KMAX; ++k)
           if (e[k] >= 0) atomicOr(&ebits[warp * E + e[k]], 1u << lane);
       }
-      const uint32_t lo = static_cast<uint32_t>(dmask), hi = static_cast<uint32_t>(dmask >> 32);
-      for (int d = 0; d < R; ++d) {
-        const uint32_t b = __ballot_sync(kFullMask, ((d < 32 ? lo : hi) >> (d & 31)) & 1u);
-        if (lane == 0) bal[warp][d] = b;
+      // lane d stores the warp's ballot of destination d (and d + 32)
+      const uint32_t col_lo = warp_transpose32(static_cast<uint32_t>(dmask), lane);
+      if (lane < R) bal[warp][lane] = col_lo;
+      if (R > 32) {
+        const uint32_t col_hi = warp_transpose32(static_cast<uint32_t>(dmask >> 32), lane);
+        if (lane + 32 < R) bal[warp][lane + 32] = col_hi;
       }
       __syncthreads();
       for (int d = tid; d < R; d += THREADS) {
@@ -295,12 +317,21 @@ __global__ void __launch_bounds__(THREADS) layout_kernel(LayoutArgs a) {
   __threadfence();
   for (int i = tid; i < R * R; i += THREADS) s_cnt[i] = ld_cg(a.recv_cnt + i);
   __syncthreads();
-  for (int d = tid; d < R; d += THREADS) {
-    int acc = 0;
-    for (int i = 0; i < R; ++i) {  // row block i holds source src(i)
-      const int src = a.n_so == 1 ? i : (i % a.n_so) * a.n_su + i / a.n_so;
-      acc += s_cnt[d * R + src];
-      a.recv_psum[d * R + i] = acc;
+  // one warp per destination: inclusive scan over the row blocks, 32 at a time
+  for (int d = warp; d < R; d += WARPS) {
+    int carry = 0;
+    for (int i0 = 0; i0 < R; i0 += 32) {
+      const int i = i0 + lane;  // row block i holds source src(i)
+      int v = 0;
+      if (i < R) v = s_cnt[d * R + (a.n_so == 1 ? i : (i % a.n_so) * a.n_su + i / a.n_so)];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(kFullMask, v, o);
+        if (lane >= o) v += u;
+      }
+      v += carry;
+      if (i < R) a.recv_psum[d * R + i] = v;
+      carry = __shfl_sync(kFullMask, v, 31);
     }
   }
   if (tid == 0) *a.done = 0u;  // ready for the next call
