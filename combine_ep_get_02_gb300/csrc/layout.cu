@@ -153,10 +153,20 @@ __global__ void __launch_bounds__(THREADS) layout_kernel(LayoutArgs a) {
 
   // ---- pass 1: this CTA's counts per destination and per expert
   bool bad = false;
+  // the first round's lanes stay in registers for pass 2 (with up to 8 lanes a
+  // token; wider tokens are loaded again)
+  constexpr bool kKeep = KMAX <= 8;
+  int e_first[kKeep ? KMAX : 1];
+  uint64_t dmask_first = 0;
   {
     int e[KMAX];
     int t = t_begin + tid;
     uint64_t dmask = load_token<KMAX>(a, tok_base + t, t < t_end, e, &bad);
+    if constexpr (kKeep) {
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k) e_first[k] = e[k];
+      dmask_first = dmask;
+    }
     for (int t0 = t_begin; t0 < t_end; t0 += THREADS) {
       // the next round's lanes are in flight while this round is counted
       int en[KMAX];
@@ -213,7 +223,14 @@ __global__ void __launch_bounds__(THREADS) layout_kernel(LayoutArgs a) {
     int e[KMAX];
     bool unused = false;
     int t = t_begin + tid;
-    uint64_t dmask = load_token<KMAX>(a, tok_base + t, t < t_end, e, &unused);
+    uint64_t dmask;
+    if constexpr (kKeep) {
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k) e[k] = e_first[k];
+      dmask = dmask_first;
+    } else {
+      dmask = load_token<KMAX>(a, tok_base + t, t < t_end, e, &unused);
+    }
     for (int t0 = t_begin; t0 < t_end; t0 += THREADS) {
       const bool live = t < t_end;
       int en[KMAX];
@@ -409,11 +426,23 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_expand_kernel(LayoutArg
   const int t_begin = min(a.T, c * a.TB), t_end = min(a.T, t_begin + a.TB);
   const int64_t i0 = (static_cast<int64_t>(s) * a.T + t_begin) * a.K;
   const int64_t i1 = (static_cast<int64_t>(s) * a.T + t_end) * a.K;
-  for (int64_t i = i0 + tid; i < i1; i += kLayoutThreads) {
-    const int p = a.exp_pos[i];
-    if (p >= 0) {
-      const int e = static_cast<int>(__ldg(a.topk_idx + i));
-      a.exp_pos[i] = p + blk[e] + off[e];
+  // four lanes in flight per thread: positions and experts load together
+  constexpr int kU = 4;
+  for (int64_t i = i0 + tid; i < i1; i += kU * kLayoutThreads) {
+    int p[kU];
+    int64_t ev[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int64_t j = i + u * kLayoutThreads;
+      p[u] = j < i1 ? a.exp_pos[j] : -1;
+      ev[u] = j < i1 ? __ldg(a.topk_idx + j) : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      if (p[u] >= 0) {  // a placed lane: its expert is valid
+        const int e = static_cast<int>(ev[u]);
+        a.exp_pos[i + u * kLayoutThreads] = p[u] + blk[e] + off[e];
+      }
     }
   }
 }
@@ -454,7 +483,8 @@ cudaError_t launch_layout(const Geometry& g, const LayoutArgs& args, int num_pro
   // expert bitmaps take shared memory), as many CTAs per source as one round
   // each needs, at most 8 (a portable cluster), within the prologue budget of
   // 2 CTAs per requested SM and at least one CTA per source
-  const int threads = g.expand ? 256 : 512;
+  // (top-k above 8 also takes 256: 32 lanes a token do not fit 512 threads' registers)
+  const int threads = (g.expand || g.K > 8) ? 256 : 512;
   const int sms = num_prologue_sms > 0 ? (num_prologue_sms < kMaxPrologueCtas ? num_prologue_sms
                                                                                : kMaxPrologueCtas)
                                        : kMaxPrologueCtas;
@@ -469,7 +499,7 @@ cudaError_t launch_layout(const Geometry& g, const LayoutArgs& args, int num_pro
   if (g.expand)
     err = g.K <= 8 ? launch_main<8, 256>(g, a, stream) : launch_main<32, 256>(g, a, stream);
   else
-    err = g.K <= 8 ? launch_main<8, 512>(g, a, stream) : launch_main<32, 512>(g, a, stream);
+    err = g.K <= 8 ? launch_main<8, 512>(g, a, stream) : launch_main<32, 256>(g, a, stream);
   if (err != cudaSuccess) return err;
   if (g.expand) {
     layout_expert_scan_kernel<<<(g.E + 31) / 32, kLayoutThreads, 0, stream>>>(a);
