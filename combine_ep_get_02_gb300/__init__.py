@@ -21,7 +21,7 @@ import torch
 from . import _build
 
 EP_OK, EP_ERR_INVALID_ARG, EP_ERR_UNSUPPORTED, EP_ERR_WORKSPACE, EP_ERR_CUDA, EP_ERR_BAD_TOPK, \
-    EP_ERR_OVERFLOW, EP_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5, -6, -7
+    EP_ERR_OVERFLOW, EP_ERR_TIMEOUT, EP_ERR_BOUNDS = 0, -1, -2, -3, -4, -5, -6, -7, -8
 EP_DTYPE_BF16, EP_DTYPE_FP8_E4M3 = 0, 1
 
 __all__ = [
@@ -29,7 +29,7 @@ __all__ = [
     "ep_workspace_init", "ep_get_dispatch_layout", "ep_get_dispatch_layout_noalloc", "ep_dispatch", "ep_combine", "ep_check_error",
     "ep_dispatch_atomic", "ep_deterministic_sort",
     "ep_status_string", "ep_diag_e4m3_of_bits", "ep_diag_bf16_of_bits",
-    "ep_diag_copy_fanout", "ep_diag_wait_timeout", "alloc_layout", "alloc_recv",
+    "ep_diag_copy_fanout", "ep_diag_wait_timeout", "use_checked", "alloc_layout", "alloc_recv",
     "alloc_workspace", "config_of",
 ]
 
@@ -101,16 +101,26 @@ def config_of(wl, **over) -> Config:
 
 
 _lib = None
+_checked = False
+
+
+def use_checked(on: bool = True) -> None:
+    """Route every later call to the bounds-checked build of the library (each
+    computed row index is tested against its buffer; one outside is skipped and
+    reported as EP_ERR_BOUNDS by ep_check_error), or back to the normal one."""
+    global _lib, _checked
+    _checked, _lib = bool(on), None
 
 
 def lib():
     """The loaded library. Raises if it has not been built (no fallback)."""
     global _lib
     if _lib is None:
-        if not os.path.exists(_build.LIB):
-            raise RuntimeError(f"CUDA library {_build.LIB} is missing: build it with "
+        path = _build.LIB_CHECKED if _checked else _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(f"CUDA library {path} is missing: build it with "
                                "`python -c 'import __graft_entry__ as g; g.build()'`")
-        L = C.CDLL(_build.LIB)
+        L = C.CDLL(path)
         P, I = C.c_void_p, C.c_int
         L.ep_workspace_bytes.restype = C.c_size_t
         L.ep_workspace_bytes.argtypes = [P]

@@ -15,6 +15,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIB_DIR, "libep_get.so")
+# the same library with every computed row index checked against its buffer
+# (-DEP_CHECKED): for tests; an index outside latches EP_ERR_BOUNDS
+LIB_CHECKED = os.path.join(LIB_DIR, "libep_get_checked.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-I", INCLUDE, "-I", CSRC,
          "--expt-relaxed-constexpr"]
@@ -70,19 +73,22 @@ def source_hash(kernel: str = None) -> str:
     return h.hexdigest()[:16]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    if not force and up_to_date():
-        return LIB
+def build(force: bool = False, verbose: bool = False, extra_flags=(), checked: bool = False) -> str:
+    lib = LIB_CHECKED if checked else LIB
+    if not force and up_to_date(lib):
+        return lib
     nvcc = _nvcc()
-    obj_dir = os.path.join(LIB_DIR, "obj")
+    obj_dir = os.path.join(LIB_DIR, "obj_checked" if checked else "obj")
     os.makedirs(obj_dir, exist_ok=True)
+    if checked:
+        extra_flags = (*extra_flags, "-DEP_CHECKED")
 
     def compile_one(src):
         obj = os.path.join(obj_dir, os.path.basename(src) + ".o")
@@ -96,13 +102,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with concurrent.futures.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, sources()))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -260,6 +260,7 @@ int ep_dispatch(const ep_config_t* cfg, const ep_layout_t* layout, const void* x
   a.recv_w = recv->recv_topk_weights;
   a.recv_md = recv->recv_src_metadata;
   a.err = at<uint32_t>(workspace, workspace_layout(g).err);
+  a.recv_rows = recv->recv_x_rows;
   a.R = g.R;
   a.E = g.E;
   a.L = g.L;
@@ -307,6 +308,8 @@ int ep_combine(const ep_config_t* cfg, const ep_layout_t* layout, const uint16_t
   a.exp_region = layout->exp_region;
   a.recv_psum = layout->recv_psum;
   a.out = out;
+  a.err = at<uint32_t>(workspace, workspace_layout(g).err);
+  a.y_rows = ep_recv_rows(cfg);
   a.E = g.E;
   a.L = g.L;
   a.K = g.K;
@@ -351,6 +354,7 @@ int ep_dispatch_atomic(const ep_config_t* cfg, const void* x, const float* x_sf,
   a.recv_idx = recv->recv_topk_idx;
   a.recv_w = recv->recv_topk_weights;
   a.recv_md = recv->recv_src_metadata;
+  a.recv_rows = recv->recv_x_rows;
   a.R = g.R;
   a.E = g.E;
   a.L = g.L;
@@ -425,6 +429,7 @@ int ep_check_error(void* workspace, void* stream) {
   if (bits & kErrBadTopk) return EP_ERR_BAD_TOPK;
   if (bits & kErrOverflow) return EP_ERR_OVERFLOW;
   if (bits & kErrTimeout) return EP_ERR_TIMEOUT;
+  if (bits & kErrBounds) return EP_ERR_BOUNDS;
   return EP_OK;
 }
 
@@ -438,6 +443,7 @@ const char* ep_status_string(int status) {
     case EP_ERR_BAD_TOPK: return "EP_ERR_BAD_TOPK";
     case EP_ERR_OVERFLOW: return "EP_ERR_OVERFLOW";
     case EP_ERR_TIMEOUT: return "EP_ERR_TIMEOUT";
+    case EP_ERR_BOUNDS: return "EP_ERR_BOUNDS";
     default: return "EP_ERR_UNKNOWN";
   }
 }

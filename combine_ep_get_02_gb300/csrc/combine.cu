@@ -63,8 +63,10 @@ __global__ void __launch_bounds__(kCopyThreads) combine_kernel(CombineArgs a) {
             kExpand ? static_cast<int64_t>(a.exp_region[d]) + r
                     : static_cast<int64_t>(d) * a.region_rows +
                           recv_row_of_slot(r, d, a.R, a.M, a.compact, a.recv_psum);
-        p = a.y + row * a.H;
-        w = w_cur;
+        if (row_in_bounds(row, a.y_rows, a.err)) {  // checked builds: the lane is dropped
+          p = a.y + row * a.H;
+          w = w_cur;
+        }
       }
       s_ptr[warp][lane] = p;
       s_w[warp][lane] = w;

@@ -41,8 +41,9 @@ __global__ void __launch_bounds__(kCopyThreads) dispatch_kernel(DispatchArgs a) 
     const TokenLanes ln = lanes_of(a, cur, tok, lane, kExpand, kAtomic);
     const unsigned hmask = kExpand ? ln.vmask : ln.rmask;
     if ((hmask >> lane) & 1) {
-      const int64_t row = kExpand ? static_cast<int64_t>(a.exp_region[ln.d]) + ln.pos
-                                  : static_cast<int64_t>(ln.d) * a.region_rows + ln.row;
+      int64_t row = kExpand ? static_cast<int64_t>(a.exp_region[ln.d]) + ln.pos
+                            : static_cast<int64_t>(ln.d) * a.region_rows + ln.row;
+      if (!row_in_bounds(row, a.recv_rows, a.err)) row = -1;  // checked builds: skipped below
       s_row[warp][__popc(hmask & lt)] = row;
     }
     __syncwarp();
@@ -60,6 +61,7 @@ __global__ void __launch_bounds__(kCopyThreads) dispatch_kernel(DispatchArgs a) 
           if (c < nchunk) v[u] = ld_stream16(src + (static_cast<size_t>(c) << 4));
         }
         for (int j = 0; j < nh; ++j) {
+          if (kChecked && s_row[warp][j] < 0) continue;
           uint8_t* dst = a.recv_x + s_row[warp][j] * a.out_row_bytes;
 #pragma unroll
           for (int u = 0; u < kUnroll; ++u) {
@@ -72,7 +74,8 @@ __global__ void __launch_bounds__(kCopyThreads) dispatch_kernel(DispatchArgs a) 
         const float* ssrc = a.x_sf + tok * a.SW;
         for (int g = lane; g < a.SW; g += 32) {
           const float v = ssrc[g];
-          for (int j = 0; j < nh; ++j) a.recv_sf[s_row[warp][j] * a.SW + g] = v;
+          for (int j = 0; j < nh; ++j)
+            if (!kChecked || s_row[warp][j] >= 0) a.recv_sf[s_row[warp][j] * a.SW + g] = v;
         }
       }
     } else {
@@ -102,7 +105,8 @@ __global__ void __launch_bounds__(kCopyThreads) dispatch_kernel(DispatchArgs a) 
               else s_sf[warp][u >> 3] = cu.sf;
             }
             for (int j = 0; j < nh; ++j)
-              st16(a.recv_x + s_row[warp][j] * a.out_row_bytes + (static_cast<size_t>(u) << 4), q);
+              if (!kChecked || s_row[warp][j] >= 0)
+                st16(a.recv_x + s_row[warp][j] * a.out_row_bytes + (static_cast<size_t>(u) << 4), q);
           }
         }
       }
@@ -115,12 +119,14 @@ __global__ void __launch_bounds__(kCopyThreads) dispatch_kernel(DispatchArgs a) 
           for (int i = 0; i < 4; ++i)
             if (4 * wd + i < a.G) v |= static_cast<uint32_t>(b[4 * wd + i]) << (8 * i);
           for (int j = 0; j < nh; ++j)
-            reinterpret_cast<uint32_t*>(a.recv_sf)[s_row[warp][j] * a.SW + wd] = v;
+            if (!kChecked || s_row[warp][j] >= 0)
+              reinterpret_cast<uint32_t*>(a.recv_sf)[s_row[warp][j] * a.SW + wd] = v;
         }
       } else {
         for (int g = lane; g < a.G; g += 32) {
           const float v = s_sf[warp][g];
-          for (int j = 0; j < nh; ++j) a.recv_sf[s_row[warp][j] * a.G + g] = v;
+          for (int j = 0; j < nh; ++j)
+            if (!kChecked || s_row[warp][j] >= 0) a.recv_sf[s_row[warp][j] * a.G + g] = v;
         }
       }
     }

@@ -77,8 +77,9 @@ __global__ void __launch_bounds__(kBulkThreads) dispatch_bulk_kernel(DispatchArg
     const TokenLanes ln = lanes_of(a, cur, tok, lane, kExpand, false);
     const unsigned hmask = kExpand ? ln.vmask : ln.rmask;
     if ((hmask >> lane) & 1) {
-      const int64_t row = kExpand ? static_cast<int64_t>(a.exp_region[ln.d]) + ln.pos
-                                  : static_cast<int64_t>(ln.d) * a.region_rows + ln.row;
+      int64_t row = kExpand ? static_cast<int64_t>(a.exp_region[ln.d]) + ln.pos
+                            : static_cast<int64_t>(ln.d) * a.region_rows + ln.row;
+      if (!row_in_bounds(row, a.recv_rows, a.err)) row = -1;  // checked builds: skipped below
       s_row[warp][__popc(hmask & lt)] = row;
     }
     __syncwarp();
@@ -103,7 +104,8 @@ __global__ void __launch_bounds__(kBulkThreads) dispatch_bulk_kernel(DispatchArg
         const int off = piece * stage_bytes;
         const uint32_t n = static_cast<uint32_t>(min(stage_bytes, row_bytes - off));
         for (int j = 0; j < nh; ++j)
-          bulk_store(a.recv_x + s_row[warp][j] * a.out_row_bytes + off, st_addr(stage), n);
+          if (!kChecked || s_row[warp][j] >= 0)
+            bulk_store(a.recv_x + s_row[warp][j] * a.out_row_bytes + off, st_addr(stage), n);
         bulk_commit();
       }
       stage ^= 1;
@@ -114,7 +116,8 @@ __global__ void __launch_bounds__(kBulkThreads) dispatch_bulk_kernel(DispatchArg
       const float* ssrc = a.x_sf + tok * a.SW;
       for (int g = lane; g < a.SW; g += 32) {
         const float v = ssrc[g];
-        for (int j = 0; j < nh; ++j) a.recv_sf[s_row[warp][j] * a.SW + g] = v;
+        for (int j = 0; j < nh; ++j)
+          if (!kChecked || s_row[warp][j] >= 0) a.recv_sf[s_row[warp][j] * a.SW + g] = v;
       }
     }
     write_sidecars(a, ln, s_rank, t, lane, kExpand);

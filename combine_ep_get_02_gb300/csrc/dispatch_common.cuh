@@ -135,6 +135,8 @@ __device__ __forceinline__ void write_sidecars(const DispatchArgs& a, const Toke
       const int dj = __shfl_sync(kFullMask, ln.d, rl);
       const int row = __shfl_sync(kFullMask, kExpand ? ln.slot : ln.row, rl);
       const int64_t mrow = static_cast<int64_t>(dj) * a.region_rows + row;
+      if (!row_in_bounds(mrow, static_cast<int64_t>(a.R) * a.region_rows, lane == 0 ? a.err : nullptr))
+        continue;  // checked builds only; the same for every lane
       if (lane < a.K) {
         const bool on = ln.d == dj;
         if (a.recv_idx) a.recv_idx[mrow * a.K + lane] = on ? static_cast<int64_t>(ln.e - dj * a.L) : -1;
@@ -152,7 +154,8 @@ __device__ __forceinline__ void write_sidecars(const DispatchArgs& a, const Toke
         if (lane + 32 < a.K + 2) md[lane + 32] = (kExpand && f1_d == dj) ? f1_pos : -1;
       }
     }
-  }}
+  }
+}
 
 // Expanded blocks padded to expert_alignment: zero the rows after each
 // expert's lanes up to the next block start (and their scales). Warp gwarp of
@@ -166,6 +169,7 @@ __device__ __forceinline__ void zero_padding_rows(const DispatchArgs& a, int64_t
     const int64_t region = a.exp_region[d];
     const int64_t first = region + a.exp_base[d * (a.L + 1) + j] + a.exp_cnt[blk];
     const int64_t end = region + a.exp_base[d * (a.L + 1) + j + 1];
+    if (end > first && !row_in_bounds(end - 1, a.recv_rows, lane == 0 ? a.err : nullptr)) continue;
     for (int64_t row = first; row < end; ++row) {
       uint8_t* dst = a.recv_x + row * a.out_row_bytes;
       for (int c = lane; c < nchunk; c += 32) st16(dst + (static_cast<size_t>(c) << 4), zero);

@@ -25,6 +25,16 @@ constexpr int kMaxSortRows = 8192;   // rows of one segment the comparison sort 
 constexpr uint32_t kErrBadTopk = 1u;
 constexpr uint32_t kErrOverflow = 2u;
 constexpr uint32_t kErrTimeout = 4u;  // a bounded wait on a copy gave up
+constexpr uint32_t kErrBounds = 8u;   // checked builds: a computed row fell outside its buffer
+
+// Checked builds (-DEP_CHECKED, libep_get_checked.so) test every computed row
+// index against its buffer before the access; one outside latches kErrBounds
+// and the access is skipped. Ordinary builds compile the tests away.
+#ifdef EP_CHECKED
+constexpr bool kChecked = true;
+#else
+constexpr bool kChecked = false;
+#endif
 
 // Sizes derived from an ep_config_t that passed validation.
 struct Geometry {
@@ -86,7 +96,8 @@ struct DispatchArgs {
   int64_t* recv_idx;
   float* recv_w;
   int32_t* recv_md;
-  uint32_t* err;             // the workspace's device error bits
+  uint32_t* err;             // the workspace's device error bits (null: none)
+  int64_t recv_rows;         // rows of recv_x and recv_sf (checked builds)
   int R, E, L, K, T, H, G, M, compact, zero_padding, n_so, n_su, sf_pack;
   int SW;  // 32-bit words of one row's scale sidecar
   int64_t region_rows;
@@ -122,6 +133,8 @@ struct CombineArgs {
   const int32_t* exp_region;
   const int32_t* recv_psum;  // compact receive rows only
   uint16_t* out;
+  uint32_t* err;     // the workspace's device error bits
+  int64_t y_rows;    // rows of y (checked builds)
   int E, L, K, T, H, R, M, compact;
   int splits;        // column ranges per token (work units per token)
   int split_chunks;  // 16-byte chunks per range
@@ -154,6 +167,14 @@ __device__ __forceinline__ int recv_row_of_slot(int slot, int d, int R, int M, i
   const int rb = slot / M;
   const int before = rb == 0 ? 0 : __ldg(recv_psum + d * R + rb - 1);
   return before + slot - rb * M;
+}
+
+// Checked builds: is row inside [0, rows)? If not, latch kErrBounds (when there
+// is an error word) and tell the caller to skip the access.
+__device__ __forceinline__ bool row_in_bounds(int64_t row, int64_t rows, uint32_t* err) {
+  if (!kChecked || (row >= 0 && row < rows)) return true;
+  if (err != nullptr) atomicOr(err, kErrBounds);
+  return false;
 }
 
 }  // namespace ep

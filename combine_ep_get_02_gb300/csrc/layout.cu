@@ -269,6 +269,8 @@ __global__ void __launch_bounds__(THREADS) layout_kernel(LayoutArgs a) {
           if (e[k] >= 0) {
             const int d = div_l(e[k], a.l_magic);
             slot[k] = wbase[warp][d] + __popc(bal[warp][d] & lt);
+            // checked builds: the slot stays inside this source's row block
+            if (!row_in_bounds(slot[k] - static_cast<int64_t>(rb) * a.M, a.M, a.err)) slot[k] = -1;
             if (a.expand) {
               int p = run_e[e[k]] + __popc(ebits[warp * E + e[k]] & lt);
               for (int w = 0; w < warp; ++w) p += __popc(ebits[w * E + e[k]]);
@@ -441,7 +443,10 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_expand_kernel(LayoutArg
     for (int u = 0; u < kU; ++u) {
       if (p[u] >= 0) {  // a placed lane: its expert is valid
         const int e = static_cast<int>(ev[u]);
-        a.exp_pos[i + u * kLayoutThreads] = p[u] + blk[e] + off[e];
+        int row = p[u] + blk[e] + off[e];
+        // checked builds: the row stays inside its destination's region
+        if (!row_in_bounds(row, size_d[e / L], a.err)) row = -1;
+        a.exp_pos[i + u * kLayoutThreads] = row;
       }
     }
   }

@@ -52,6 +52,10 @@ extern "C" {
 #define EP_ERR_TIMEOUT (-7)     /* device: a bounded wait for a bulk copy gave
                                    up (the kernel returned early; its
                                    outputs are incomplete)                   */
+#define EP_ERR_BOUNDS (-8)      /* device, checked builds only
+                                   (libep_get_checked.so): a computed row
+                                   index fell outside its buffer; that access
+                                   was skipped                               */
 
 /* ---- element types ------------------------------------------------------- */
 #define EP_DTYPE_BF16 0

@@ -26,6 +26,18 @@ def declared_functions():
     return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\**\s*(ep_[a-z_0-9]+)\s*\(", text, flags=re.M)))
 
 
+def test_checked_build_exports_the_same_symbols(ep):
+    ep._build.build(checked=True)
+    names = declared_functions()
+    nm = subprocess.run(["nm", "-D", "--defined-only", ep._build.LIB_CHECKED], capture_output=True,
+                        text=True).stdout
+    exported = set(re.findall(r"\sT\s(\w+)", nm))
+    assert set(names) <= exported
+    lib = C.CDLL(ep._build.LIB_CHECKED)
+    for n in names:
+        getattr(lib, n)
+
+
 def test_every_declared_symbol_is_exported(ep):
     names = declared_functions()
     assert {"ep_get_dispatch_layout", "ep_dispatch", "ep_combine", "ep_workspace_bytes",
