@@ -9,7 +9,14 @@ all logical ranks per second) and the HBM bandwidth each phase achieves.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
     python bench.py --impl reference ...   # the CPU oracle, timed on the host
 
-Prints one JSON line (rank 0).
+Prints one JSON line (rank 0). Beside the contract keys it carries `phases`
+(per-phase time, algorithmic bytes, GB/s and fraction of the measured copy
+peak), `roofline` (the dominant kernel, with ncu DRAM traffic when the committed
+capture matches the kernel's sources), `graph` (the same step replayed as one
+CUDA graph), `dispatch_ceiling` (a one-read, many-write copy of the dispatch's
+own bytes, register and bulk methods: the ceiling of that access pattern), `e2e`
+(the step through the ABI from pinned host buffers, with the transfers alone
+beside it) and `cpu_baseline` (the oracle on one host core).
 """
 from __future__ import annotations
 
