@@ -59,8 +59,25 @@ class _Recv(C.Structure):
                 ("recv_x_rows", C.c_int64)]
 
 
+class _KeepsStruct:
+    """Keeps the ctypes struct built by _c() until a field is assigned again, so
+    a call reuses it instead of marshalling every field (the struct holds the
+    values, and for tensors their data pointers, as of that build)."""
+
+    def __setattr__(self, name, value):
+        object.__setattr__(self, name, value)
+        object.__setattr__(self, "_struct", None)
+
+    def _c(self):
+        st = self.__dict__.get("_struct")
+        if st is None:
+            st = self._build_struct()
+            object.__setattr__(self, "_struct", st)
+        return st
+
+
 @dataclasses.dataclass
-class Config:
+class Config(_KeepsStruct):
     num_scaleout_ranks: int
     num_scaleup_ranks: int
     num_experts: int
@@ -83,7 +100,7 @@ class Config:
     def num_ranks(self) -> int:
         return self.num_scaleout_ranks * self.num_scaleup_ranks
 
-    def _c(self) -> _Config:
+    def _build_struct(self) -> _Config:
         return _Config(*(int(getattr(self, f[0])) for f in _Config._fields_))
 
 
@@ -191,7 +208,7 @@ def ep_workspace_init(ws: torch.Tensor, stream=None):
 
 
 @dataclasses.dataclass
-class Layout:
+class Layout(_KeepsStruct):
     num_tokens_per_rank: torch.Tensor
     num_tokens_per_expert: torch.Tensor
     is_token_in_rank: torch.Tensor
@@ -203,19 +220,19 @@ class Layout:
     exp_region: torch.Tensor | None = None
     exp_pos: torch.Tensor | None = None
 
-    def _c(self) -> _Layout:
+    def _build_struct(self) -> _Layout:
         return _Layout(*(_ptr(getattr(self, f[0])) for f in _Layout._fields_))
 
 
 @dataclasses.dataclass
-class Recv:
+class Recv(_KeepsStruct):
     recv_x: torch.Tensor
     recv_sf: torch.Tensor | None
     recv_topk_idx: torch.Tensor | None
     recv_topk_weights: torch.Tensor | None
     recv_src_metadata: torch.Tensor | None
 
-    def _c(self) -> _Recv:
+    def _build_struct(self) -> _Recv:
         return _Recv(_ptr(self.recv_x), _ptr(self.recv_sf), _ptr(self.recv_topk_idx),
                      _ptr(self.recv_topk_weights), _ptr(self.recv_src_metadata), self.recv_x.shape[0])
 

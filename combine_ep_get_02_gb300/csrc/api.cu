@@ -6,6 +6,9 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <mutex>
+#include <vector>
+
 #include "ep_device.cuh"
 #include "ep_internal.cuh"
 
@@ -42,6 +45,45 @@ __global__ void diag_bf16_kernel(uint32_t first, int64_t n, uint16_t* out) {
 }
 
 }  // namespace
+
+int resident_ctas(const void* kernel, int threads, size_t smem) {
+  struct Known {
+    const void* kernel;
+    int threads;
+    size_t smem;
+    int device;
+    int ctas;
+  };
+  struct Limit {  // the largest dynamic shared-memory limit set on a kernel so far
+    const void* kernel;
+    int device;
+    size_t smem;
+  };
+  static std::mutex mu;
+  static std::vector<Known> known;
+  static std::vector<Limit> limits;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  std::lock_guard<std::mutex> lock(mu);
+  if (smem > 48 * 1024) {  // raise the kernel's limit when this launch needs more; never lower it
+    Limit* lim = nullptr;
+    for (Limit& l : limits)
+      if (l.kernel == kernel && l.device == dev) lim = &l;
+    if (lim == nullptr || lim->smem < smem) {
+      if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+          cudaSuccess)
+        return -1;
+      if (lim == nullptr) limits.push_back({kernel, dev, smem});
+      else lim->smem = smem;
+    }
+  }
+  for (const Known& e : known)
+    if (e.kernel == kernel && e.threads == threads && e.smem == smem && e.device == dev) return e.ctas;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess) return -1;
+  known.push_back({kernel, threads, smem, dev, n});
+  return n;
+}
 
 int device_sm_count() {
   int dev = 0, n = 0;

@@ -122,9 +122,8 @@ __global__ void __launch_bounds__(kCopyThreads) combine_kernel(CombineArgs a) {
 template <bool kExpand, int kMaxK, int kSteps>
 cudaError_t launch_one(const CombineArgs& args, int num_sms, cudaStream_t stream) {
   auto kern = combine_kernel<kExpand, kMaxK, kSteps>;
-  int per_sm = 0;
-  cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kCopyThreads, 0);
-  if (err != cudaSuccess) return err;
+  int per_sm = resident_ctas(reinterpret_cast<const void*>(kern), kCopyThreads, 0);
+  if (per_sm < 0) return cudaErrorUnknown;
   if (per_sm < 1) per_sm = 1;
   CombineArgs a = args;
   // Split tokens into column ranges until every warp gets about 16 units, so

@@ -142,9 +142,8 @@ __global__ void __launch_bounds__(kCopyThreads) dispatch_kernel(DispatchArgs a) 
 template <int kKind, bool kExpand, bool kAtomic = false>
 cudaError_t launch_one(const DispatchArgs& a, int num_sms, cudaStream_t stream) {
   auto kern = dispatch_kernel<kKind, kExpand, kAtomic>;
-  int per_sm = 0;
-  cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kCopyThreads, 0);
-  if (err != cudaSuccess) return err;
+  int per_sm = resident_ctas(reinterpret_cast<const void*>(kern), kCopyThreads, 0);
+  if (per_sm < 0) return cudaErrorUnknown;
   if (per_sm < 1) per_sm = 1;
   int64_t ctas = static_cast<int64_t>(num_sms) * per_sm;
   const int64_t need = ((a.zero_padding && a.E > a.num_tokens ? a.E : a.num_tokens) + kWarps - 1) / kWarps;

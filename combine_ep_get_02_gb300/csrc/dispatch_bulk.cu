@@ -149,11 +149,8 @@ cudaError_t launch_dispatch_bulk(const Geometry& g, const DispatchArgs& a, int n
   const int stage_bytes = dispatch_bulk_stage_bytes(a.in_row_bytes);
   const size_t smem = static_cast<size_t>(kBulkWarps) * kBulkStages * stage_bytes;
   auto kern = g.expand ? dispatch_bulk_kernel<true> : dispatch_bulk_kernel<false>;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-  if (err != cudaSuccess) return err;
-  int per_sm = 0;
-  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kBulkThreads, smem);
-  if (err != cudaSuccess) return err;
+  int per_sm = resident_ctas(reinterpret_cast<const void*>(kern), kBulkThreads, smem);
+  if (per_sm < 0) return cudaErrorUnknown;
   if (per_sm > kBulkMaxCtasPerSm) per_sm = kBulkMaxCtasPerSm;
   if (per_sm < 1) per_sm = 1;
   int64_t ctas = static_cast<int64_t>(num_sms) * per_sm;

@@ -158,6 +158,14 @@ cudaError_t launch_combine(const Geometry& g, const CombineArgs& a, int num_sms,
 
 int device_sm_count();
 
+// Resident CTAs per SM of `kernel` at `threads` threads and `smem` bytes of
+// dynamic shared memory on the current device, raising the kernel's dynamic
+// shared-memory limit first when smem needs it. Asked of the runtime once per
+// (kernel, threads, smem, device) and kept, so a launch pays for neither query
+// again; the limit is only ever raised. Returns the count (>= 0) or -1 if a
+// runtime call failed.
+int resident_ctas(const void* kernel, int threads, size_t smem);
+
 // Receive row inside destination d's region of a row-form slot: the slot, or
 // (compact) the exclusive prefix of d's receive counts before the slot's row
 // block plus the slot's offset in that block.
