@@ -15,8 +15,8 @@ peak), `roofline` (the dominant kernel, with ncu DRAM traffic when the committed
 capture matches the kernel's sources), `graph` (the same step replayed as one
 CUDA graph), `dispatch_ceiling` (a one-read, many-write copy of the dispatch's
 own bytes, register and bulk methods: the ceiling of that access pattern), `e2e`
-(the step through the ABI from pinned host buffers, with the transfers alone
-beside it) and `cpu_baseline` (the oracle on one host core).
+(the step through the ABI from pinned host buffers; `--host-link` times the
+same copies alone, its bound) and `cpu_baseline` (the oracle on one host core).
 """
 from __future__ import annotations
 
@@ -67,6 +67,8 @@ def parse():
     p.add_argument("--compare-sort", action="store_true",
                    help="time the deterministic dispatch against atomic slots + post-hoc sort")
     p.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
+    p.add_argument("--host-link", action="store_true",
+                   help="only time one step's host<->device copies (the end-to-end bound), nothing else")
     p.add_argument("--no-ceiling", action="store_true",
                    help="skip the one-read, many-write copy timed at the dispatch's byte counts")
     p.add_argument("--no-e2e", action="store_true")
@@ -520,29 +522,32 @@ def end_to_end(ep, cfg, wl, idx_h, w_h, x_h, sf_h, lay, recv, y, identity, ws, s
         (0 if hsf is None else hsf.numel() * 4)
     d2h = hout[0].numel() * 2
 
-    link_ms = transfer_only_ms(hx, hidx, hw, hsf, dx[0], didx[0], dw[0], dsf[0], hout[1], dout[1], stream, dev)
     return {"value": whole_job_rate(world, R * T, ms * steps, steps), "unit": "tokens/s",
             "ms_per_step": ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "steps": steps, "transfer_only_ms_per_step": link_ms,
+            "steps": steps,
             "pipeline": "double-buffered host copies on two copy streams, overlapped with the kernels"}
 
 
-def transfer_only_ms(hx, hidx, hw, hsf, dx, didx, dw, dsf, hout, dout, stream, dev, reps=5):
-    """One step's input copied in and its output copied back at the same time,
-    with no kernels: the host link's bound on the end-to-end step."""
+def transfer_only_ms(hx, hidx, hw, hsf, dx, didx, dw, dsf, hout, dout, stream, dev, reps=5,
+                     inputs=True, output=True):
+    """One step's input copied in and/or its output copied back (at the same
+    time when both), with no kernels: the host link's bound on the end-to-end
+    step."""
     t_in, t_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
     def once():
         t_in.wait_stream(stream)
         t_out.wait_stream(stream)
-        with torch.cuda.stream(t_in):
-            dx.copy_(hx, non_blocking=True)
-            didx.copy_(hidx, non_blocking=True)
-            dw.copy_(hw, non_blocking=True)
-            if dsf is not None:
-                dsf.copy_(hsf, non_blocking=True)
-        with torch.cuda.stream(t_out):
-            hout.copy_(dout, non_blocking=True)
+        if inputs:
+            with torch.cuda.stream(t_in):
+                dx.copy_(hx, non_blocking=True)
+                didx.copy_(hidx, non_blocking=True)
+                dw.copy_(hw, non_blocking=True)
+                if dsf is not None:
+                    dsf.copy_(hsf, non_blocking=True)
+        if output:
+            with torch.cuda.stream(t_out):
+                hout.copy_(dout, non_blocking=True)
         stream.wait_stream(t_in)
         stream.wait_stream(t_out)
 
@@ -555,6 +560,29 @@ def transfer_only_ms(hx, hidx, hw, hsf, dx, didx, dw, dsf, hout, dout, stream, d
     b.record(stream)
     torch.cuda.synchronize(dev)
     return a.elapsed_time(b) / reps
+
+
+def host_link(args):
+    """The host-link bound of the end-to-end step, in a process that does nothing
+    else: one step's inputs in and output back (pinned host buffers), alone and
+    at the same time."""
+    dev = torch.device("cuda", 0)
+    wl = workload(args)
+    R, T, H = wl.num_ranks, wl.num_tokens, wl.hidden
+    idx_h, w_h = W.routing(wl)
+    x_h, sf_h = W.hidden(wl)
+    hx, hidx, hw = x_h.pin_memory(), idx_h.pin_memory(), w_h.pin_memory()
+    hsf = None if sf_h is None else sf_h.pin_memory()
+    dx, didx, dw = (torch.empty_like(t, device=dev) for t in (hx, hidx, hw))
+    dsf = None if hsf is None else torch.empty_like(hsf, device=dev)
+    hout = torch.empty(R, T, H, dtype=torch.bfloat16).pin_memory()
+    dout = torch.zeros(R, T, H, dtype=torch.bfloat16, device=dev)
+    st = torch.cuda.current_stream(dev)
+    f = lambda i, o: transfer_only_ms(hx, hidx, hw, hsf, dx, didx, dw, dsf, hout, dout, st, dev, inputs=i, output=o)
+    h2d = hx.numel() * hx.element_size() + hidx.numel() * 8 + hw.numel() * 4 + (0 if hsf is None else hsf.numel() * 4)
+    print(json.dumps({"mode": "host_link", "workload": describe(wl), "h2d_bytes_per_step": h2d,
+                      "d2h_bytes_per_step": hout.numel() * 2, "h2d_ms": f(True, False), "d2h_ms": f(False, True),
+                      "both_ms": f(True, True)}), flush=True)
 
 
 def ncu_traffic(kernel, wl, n_tok):
@@ -720,6 +748,8 @@ def main():
         reference(args)
     elif args.compare_sort:
         compare_sort(args)
+    elif args.host_link:
+        host_link(args)
     else:
         native(args)
 
