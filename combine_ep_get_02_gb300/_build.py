@@ -61,15 +61,24 @@ def kernel_sources(kernel: str) -> list:
     return sorted(seen)
 
 
+def _code_only(text: str) -> str:
+    """C/C++ source without comments and blank lines (what the compiler sees)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(ln.rstrip() for ln in text.splitlines() if ln.strip())
+
+
 def source_hash(kernel: str = None) -> str:
-    """Short hash of one kernel's sources (its unit and the csrc headers it
-    includes), or of every source and header when no kernel is named."""
+    """Short hash of one kernel's code (its unit and the csrc headers it
+    includes, comments left out), or of every source and header when no kernel
+    is named."""
     import hashlib
     files = kernel_sources(kernel) if kernel else [p for p in sorted(_deps()) if p.endswith((".cu", ".cuh", ".h"))]
     h = hashlib.sha256()
     for p in files:
         h.update(os.path.basename(p).encode())
-        h.update(open(p, "rb").read())
+        h.update(_code_only(open(p).read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -8,6 +8,9 @@
 // racing for them). Tokens are spread over a persistent grid sized to the SMs.
 // Lanes 0..K-1 carry the token's top-k lanes and write the small sidecar rows
 // (routing of the lanes to that destination and the source metadata).
+// This register path carries the fused cast always, and rows that travel
+// unchanged when copy_path asks for it or the input is small; larger unchanged
+// inputs go to the bulk-copy kernel in dispatch_bulk.cu.
 #include "dispatch_common.cuh"
 #include "ep_device.cuh"
 #include "ep_internal.cuh"
