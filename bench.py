@@ -320,6 +320,8 @@ def native(args):
     ms_per_step = total_ms / args.steps
     phase_ms = {name: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev)
                 for j, name in enumerate(("layout", "dispatch", "combine"))}
+    phase_med = {name: statistics.median(e[j].elapsed_time(e[j + 1]) for e in ev)
+                 for j, name in enumerate(("layout", "dispatch", "combine"))}
 
     # algorithmic bytes from this layout's counts
     ntpr = int(lay.num_tokens_per_rank.sum().item())
@@ -366,8 +368,8 @@ def native(args):
                    "copy_path": {0: "automatic", 1: "register copies", 2: "bulk copies"}[args.copy_path],
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "phases": {
-            k: {"us": phase_ms[k] * 1e3, "algorithmic_bytes": abytes[k], "gbs": gbs[k],
-                "frac_of_peak": gbs[k] / peak} for k in ("layout", "dispatch", "combine")},
+            k: {"us": phase_ms[k] * 1e3, "us_median": phase_med[k] * 1e3, "algorithmic_bytes": abytes[k],
+                "gbs": gbs[k], "frac_of_peak": gbs[k] / peak} for k in ("layout", "dispatch", "combine")},
         "roofline": {"kernel": f"{dominant}_kernel", "bound": "hbm", "achieved": gbs[dominant],
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": gbs[dominant] / peak, "traffic": ncu_traffic(f"{dominant}_kernel", wl, R * T)},
