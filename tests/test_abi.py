@@ -187,3 +187,14 @@ def test_product_path_fails_loudly_without_the_library(ep, monkeypatch):
     monkeypatch.setattr(ep._build, "LIB", "/nonexistent/libep_get.so")
     with pytest.raises(RuntimeError, match="missing"):
         ep.lib()
+
+
+def test_kernel_hash_ignores_comments_but_not_code(ep, tmp_path, monkeypatch):
+    """The ncu traffic figures are keyed by a hash of each kernel's code; a comment
+    edit keeps it, a code edit changes it."""
+    b = ep._build
+    src = open(os.path.join(b.CSRC, "combine.cu")).read()
+    assert b._code_only("int a; // note\n/* block\n comment */int b;\n\n") == "int a;\nint b;"
+    base = b._code_only(src)
+    assert b._code_only("// a new remark\n" + src.replace("\n", "\n/* x */", 1)) == base
+    assert b._code_only(src.replace("kSteps", "kStepz", 1)) != base
