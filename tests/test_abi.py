@@ -198,3 +198,13 @@ def test_kernel_hash_ignores_comments_but_not_code(ep, tmp_path, monkeypatch):
     base = b._code_only(src)
     assert b._code_only("// a new remark\n" + src.replace("\n", "\n/* x */", 1)) == base
     assert b._code_only(src.replace("kSteps", "kStepz", 1)) != base
+
+
+def test_status_codes_agree_across_header_library_and_binding(ep):
+    text = open(os.path.join(ROOT, "include", "ep_get.h")).read()
+    codes = {m.group(1): int(m.group(2)) for m in re.finditer(r"#define (EP_(?:OK|ERR_\w+))\s+\(?(-?\d+)\)?", text)}
+    assert codes["EP_OK"] == 0 and len(codes) >= 9
+    for name, value in codes.items():
+        assert getattr(ep, name) == value, name          # the binding's constant
+        assert ep.ep_status_string(value) == name         # the library's name for it
+    assert len(set(codes.values())) == len(codes)
