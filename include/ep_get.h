@@ -24,7 +24,9 @@
  *     is enqueued asynchronously on it, in call order.
  *   - Returns EP_OK (0) or a negative EP_ERR_* code. Host-detectable errors are
  *     reported before anything is enqueued. Errors found on the device (bad
- *     top-k values) are latched in the workspace and read by ep_check_error.
+ *     top-k values; a bounded wait that ran out; in the bounds-checked build
+ *     libep_get_checked.so, a row index outside its buffer) are latched in the
+ *     workspace and read by ep_check_error.
  *     Unsupported combinations return EP_ERR_UNSUPPORTED; nothing is ever
  *     dropped silently.
  *   - All row pointers must be 16-byte aligned.
@@ -226,8 +228,8 @@ int ep_dispatch(const ep_config_t* cfg, const ep_layout_t* layout, const void* x
 /* Combine: out[s][t] = bf16_rn(acc), acc = +0 then, for k in lane order over
  * the valid lanes, acc = fma(topk_weights[s][t][k], y[row of lane k], acc),
  * in fp32. y: device bf16 expert outputs in the receive layout (row form or
- * compact [R][R*M][H], or expanded [rows][H]); out: device bf16 [R][T][H]. The
- * result is bitwise reproducible. */
+ * compact [R][R*M][H], or expanded [rows][H]), at least ep_recv_rows(cfg)
+ * rows; out: device bf16 [R][T][H]. The result is bitwise reproducible. */
 int ep_combine(const ep_config_t* cfg, const ep_layout_t* layout, const uint16_t* y,
                const int64_t* topk_idx, const float* topk_weights, uint16_t* out,
                void* workspace, size_t workspace_bytes, void* stream);
