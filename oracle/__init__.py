@@ -4,12 +4,14 @@ TEST INFRASTRUCTURE ONLY. Only the tests, ``__graft_entry__.smoke()`` and the
 benchmark's CPU-baseline / reference leg may import this package; the product
 path never does. It shares no code with the CUDA library: the arithmetic lives
 in ``ep_oracle.cpp`` (plain single-threaded C++), this file only marshals numpy
-arrays. Which passage of the DeepEP pages each function follows is stated in
-``ep_oracle.cpp``.
+arrays (the row of every lane in the receive tensors, too, comes from the C++
+side: ``lane_rows``). Which passage of the DeepEP pages each function follows is
+stated in ``ep_oracle.cpp``.
 
 A workload is any object with the attributes ``n_so, n_su, num_experts,
 num_topk, num_tokens, num_max_tokens_per_rank, hidden, x_dtype, recv_dtype,
-expand, expert_alignment``.
+expand, expert_alignment`` (and optionally ``compact`` 0/1/2, ``zero_padding``,
+``sf_pack``, ``recv_capacity``).
 """
 from __future__ import annotations
 
@@ -26,7 +28,7 @@ OK, INVALID, UNSUPPORTED, BAD_TOPK, OVERFLOW = 0, -1, -2, -5, -6
 class _Cfg(C.Structure):
     _fields_ = [(n, C.c_int32) for n in
                 ("n_so", "n_su", "E", "K", "T", "M", "H", "x_fp8", "recv_fp8", "expand", "align",
-                 "compact", "zero_padding", "sf_pack")]
+                 "compact", "zero_padding", "sf_pack", "recv_capacity")]
 
 
 _lib = None
@@ -54,18 +56,22 @@ def lib():
         L.orc_cast_row_fp8_ue8m0.argtypes = [P, C.c_int, P, P]
         L.orc_recv_rows.restype = C.c_int64
         L.orc_recv_rows.argtypes = [P]
+        L.orc_sidecar_rows.restype = C.c_int64
+        L.orc_sidecar_rows.argtypes = [P]
         L.orc_layout.restype = C.c_int
-        L.orc_layout.argtypes = [P] * 12
+        L.orc_layout.argtypes = [P] * 13
         L.orc_dispatch_token.restype = C.c_int
-        L.orc_dispatch_token.argtypes = [P, C.c_int, C.c_int] + [P] * 16
+        L.orc_dispatch_token.argtypes = [P, C.c_int, C.c_int] + [P] * 18
         L.orc_dispatch.restype = C.c_int
-        L.orc_dispatch.argtypes = [P] * 16
+        L.orc_dispatch.argtypes = [P] * 17
+        L.orc_lane_rows.restype = C.c_int
+        L.orc_lane_rows.argtypes = [P] * 9
         L.orc_combine_token.restype = None
         L.orc_combine_token.argtypes = [C.c_int, C.c_int, P, P, P]
         L.orc_combine_gathered.restype = None
         L.orc_combine_gathered.argtypes = [C.c_int, C.c_int, C.c_int64, P, P, P, P]
         L.orc_combine.restype = C.c_int
-        L.orc_combine.argtypes = [P] * 9
+        L.orc_combine.argtypes = [P] * 10
         _lib = L
     return _lib
 
@@ -78,9 +84,10 @@ def cfg_of(wl) -> _Cfg:
     return _Cfg(wl.n_so, wl.n_su, wl.num_experts, wl.num_topk, wl.num_tokens,
                 wl.num_max_tokens_per_rank, wl.hidden, int(wl.x_dtype == "fp8"),
                 int(wl.recv_dtype == "fp8"), int(bool(wl.expand)), wl.expert_alignment,
-                int(bool(getattr(wl, "compact", False))),
+                int(getattr(wl, "compact", 0)),
                 int(bool(getattr(wl, "zero_padding", False))),
-                int(bool(getattr(wl, "sf_pack", False))))
+                int(bool(getattr(wl, "sf_pack", False))),
+                int(getattr(wl, "recv_capacity", 0)))
 
 
 def _np(a, dtype):
@@ -170,8 +177,15 @@ def cast_row_fp8(x_bits: np.ndarray):
 # ---- the path ----------------------------------------------------------------
 
 def recv_rows(wl) -> int:
+    """Rows of recv_x (and recv_sf)."""
     c = cfg_of(wl)
     return int(lib().orc_recv_rows(C.byref(c)))
+
+
+def sidecar_rows(wl) -> int:
+    """Rows of the sidecar tensors (recv_topk_idx, recv_topk_weights, recv_src_metadata)."""
+    c = cfg_of(wl)
+    return int(lib().orc_sidecar_rows(C.byref(c)))
 
 
 def layout(wl, topk_idx):
@@ -187,13 +201,14 @@ def layout(wl, topk_idx):
         slot_map=np.zeros((R, T, K), np.int32),
         recv_cnt=np.zeros((R, R), np.int32),
         recv_psum=np.zeros((R, R), np.int32),
+        recv_region=np.zeros(R + 1, np.int32),
     )
     if wl.expand:
         out.update(exp_cnt=np.zeros((R, L), np.int32), exp_base=np.zeros((R, L + 1), np.int32),
                    exp_region=np.zeros(R + 1, np.int32), exp_pos=np.zeros((R, T, K), np.int32))
     st = lib().orc_layout(C.byref(c), _p(idx), *(_p(out[k]) for k in (
         "num_tokens_per_rank", "num_tokens_per_expert", "is_token_in_rank", "slot_map",
-        "recv_cnt", "recv_psum")), *(_p(out.get(k)) for k in (
+        "recv_cnt", "recv_psum", "recv_region")), *(_p(out.get(k)) for k in (
         "exp_cnt", "exp_base", "exp_region", "exp_pos")))
     return st, out
 
@@ -201,9 +216,10 @@ def layout(wl, topk_idx):
 def dispatch_token(wl, lay, s, t, x_row, x_sf_row, idx_tok, w_tok):
     """Receive rows of source token (s, t). Returns a dict:
     hid (received row: uint16 bf16 bits or uint8 e4m3 codes), hid_sf,
-    hid_dst/hid_row (destinations of the hidden row; row inside the destination
-    region: slot or expanded position), meta_dst/meta_row and the sidecar rows
-    meta_idx [n,K], meta_w [n,K], meta_md [n,2+K]."""
+    hid_dst/hid_row (destinations of the hidden row and its rows of recv_x),
+    meta_dst/meta_row (deduplicated entries: destination and row of the
+    sidecar tensors) and the sidecar rows meta_idx [n,K], meta_w [n,K],
+    meta_md [n,2+K]."""
     c = cfg_of(wl)
     K, H = wl.num_topk, wl.hidden
     G = H // 128
@@ -224,7 +240,8 @@ def dispatch_token(wl, lay, s, t, x_row, x_sf_row, idx_tok, w_tok):
     slot = np.ascontiguousarray(lay["slot_map"][s, t], dtype=np.int32)
     pos = np.ascontiguousarray(lay["exp_pos"][s, t], dtype=np.int32) if wl.expand else None
     n = lib().orc_dispatch_token(
-        C.byref(c), s, t, _p(slot), _p(pos), _p(lay["recv_psum"]), _p(xr), _p(sfr),
+        C.byref(c), s, t, _p(slot), _p(pos), _p(lay["recv_psum"]), _p(lay["recv_region"]),
+        _p(lay.get("exp_region")), _p(xr), _p(sfr),
         _p(np.ascontiguousarray(idx_tok, dtype=np.int64)),
         _p(np.ascontiguousarray(w_tok, dtype=np.float32)), _p(hid), _p(hid_sf), _p(hid_dst),
         _p(hid_row), _p(meta_dst), _p(meta_row), _p(meta_idx), _p(meta_w), _p(meta_md))
@@ -238,13 +255,14 @@ def dispatch_token(wl, lay, s, t, x_row, x_sf_row, idx_tok, w_tok):
 
 def dispatch(wl, lay, x, x_sf, topk_idx, topk_weights, fill=0):
     """Full dispatch. Returns (status, dict): recv_x [rows, H] (uint16 bf16 bits or
-    uint8 e4m3 codes), recv_sf [rows, G] or None, recv_topk_idx [R, R*M, K],
-    recv_topk_weights [R, R*M, K], recv_src_metadata [R, R*M, 2+K]. Rows that no
-    entry fills keep the byte value `fill`."""
+    uint8 e4m3 codes), recv_sf [rows, G] or None, and the sidecars
+    recv_topk_idx [S, K], recv_topk_weights [S, K], recv_src_metadata [S, 2+K]
+    with S = sidecar_rows(wl). Rows that no entry fills keep the byte value
+    `fill` in every tensor."""
     c = cfg_of(wl)
-    R, K, H, M = wl.num_ranks, wl.num_topk, wl.hidden, wl.num_max_tokens_per_rank
-    G = H // 128
+    K, H = wl.num_topk, wl.hidden
     rows = recv_rows(wl)
+    S = sidecar_rows(wl)
     fp8_in = wl.x_dtype == "fp8"
     fp8_out = wl.recv_dtype == "fp8"
     xa = _np(x, np.uint8 if fp8_in else np.uint16)
@@ -253,13 +271,14 @@ def dispatch(wl, lay, x, x_sf, topk_idx, topk_weights, fill=0):
     out = dict(
         recv_x=np.full((rows, H * (1 if fp8_out else 2)), fill, np.uint8).view(np.uint8 if fp8_out else np.uint16),
         recv_sf=np.full((rows, SW * 4), fill, np.uint8).view(np.float32) if fp8_out else None,
-        recv_topk_idx=np.zeros((R, R * M, K), np.int64),
-        recv_topk_weights=np.zeros((R, R * M, K), np.float32),
-        recv_src_metadata=np.zeros((R, R * M, 2 + K), np.int32),
+        recv_topk_idx=np.full((S, K * 8), fill, np.uint8).view(np.int64),
+        recv_topk_weights=np.full((S, K * 4), fill, np.uint8).view(np.float32),
+        recv_src_metadata=np.full((S, (2 + K) * 4), fill, np.uint8).view(np.int32),
     )
     st = lib().orc_dispatch(
         C.byref(c), _p(lay["slot_map"]), _p(lay.get("exp_pos")), _p(lay.get("exp_region")),
-        _p(lay.get("exp_cnt")), _p(lay.get("exp_base")), _p(lay["recv_psum"]), _p(xa), _p(sfa), _p(_np(topk_idx, np.int64)), _p(_np(topk_weights, np.float32)),
+        _p(lay.get("exp_cnt")), _p(lay.get("exp_base")), _p(lay["recv_psum"]), _p(lay["recv_region"]),
+        _p(xa), _p(sfa), _p(_np(topk_idx, np.int64)), _p(_np(topk_weights, np.float32)),
         _p(out["recv_x"]), _p(out["recv_sf"]), _p(out["recv_topk_idx"]),
         _p(out["recv_topk_weights"]), _p(out["recv_src_metadata"]))
     return st, out
@@ -288,33 +307,25 @@ def combine_gathered(lane_rows, y, w):
     return out
 
 
-def recv_rows_of_slots(wl, lay, d, slot):
-    """Receive row (inside the destination's region) of row-form slots: the slot
-    itself, or its compact row (entries packed from row 0 in row-block order)."""
-    if not getattr(wl, "compact", False):
-        return slot
-    M, R = wl.num_max_tokens_per_rank, wl.num_ranks
-    rb = slot // M
-    psum = lay["recv_psum"].astype(np.int64)
-    before = np.where(rb > 0, psum[d, np.maximum(rb - 1, 0)], 0)
-    return before + slot - rb * M
+def lane_rows(wl, lay, topk_idx):
+    """Row of every top-k lane in the receive tensors, from the C++ oracle.
+    Returns (status, hid int64 [R,T,K], side int64 [R,T,K]): the recv_x row the
+    lane's expert reads (its deduplicated entry's row, or its expanded row) and
+    the sidecar row of its deduplicated entry; -1 for masked lanes (and, packed,
+    for entries past the capacity)."""
+    c = cfg_of(wl)
+    R, T, K = wl.num_ranks, wl.num_tokens, wl.num_topk
+    hid = np.empty((R, T, K), np.int64)
+    side = np.empty((R, T, K), np.int64)
+    st = lib().orc_lane_rows(C.byref(c), _p(_np(topk_idx, np.int64)), _p(lay["slot_map"]),
+                             _p(lay.get("exp_pos")), _p(lay.get("exp_region")), _p(lay["recv_psum"]),
+                             _p(lay["recv_region"]), _p(hid), _p(side))
+    return st, hid, side
 
 
 def global_rows(wl, lay, topk_idx):
-    """Row of every lane in the receive layout: d*R*M + row (row form or compact)
-    or exp_region[d] + exp_pos (expanded); -1 for masked lanes. int64 [R, T, K]."""
-    idx = _np(topk_idx, np.int64)
-    R = wl.num_ranks
-    L = wl.num_experts // R
-    d = np.where(idx >= 0, idx // L, 0)
-    if wl.expand:
-        r = lay["exp_region"][d].astype(np.int64) + lay["exp_pos"]
-        ok = lay["exp_pos"] >= 0
-    else:
-        slot = lay["slot_map"].astype(np.int64)
-        ok = slot >= 0
-        r = d * (R * wl.num_max_tokens_per_rank) + recv_rows_of_slots(wl, lay, d, np.maximum(slot, 0))
-    return np.where(ok & (idx >= 0), r, -1).astype(np.int64)
+    """The recv_x row of every lane (``lane_rows``' first array): int64 [R,T,K]."""
+    return lane_rows(wl, lay, topk_idx)[1]
 
 
 def combine(wl, lay, y, topk_idx, topk_weights):
@@ -325,6 +336,7 @@ def combine(wl, lay, y, topk_idx, topk_weights):
     ya = _np(y, np.uint16)
     out = np.zeros((R, T, H), np.uint16)
     st = lib().orc_combine(C.byref(c), _p(lay["slot_map"]), _p(lay.get("exp_pos")),
-                           _p(lay.get("exp_region")), _p(lay["recv_psum"]), _p(ya), _p(_np(topk_idx, np.int64)),
+                           _p(lay.get("exp_region")), _p(lay["recv_psum"]), _p(lay["recv_region"]), _p(ya),
+                           _p(_np(topk_idx, np.int64)),
                            _p(_np(topk_weights, np.float32)), _p(out))
     return st, out

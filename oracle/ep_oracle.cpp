@@ -19,7 +19,10 @@
 //     counts with their prefix sums.
 //   * PR #690 "Add Direct Recv X dispatch path", review of the copy epilogue:
 //     metadata field 2 + lane holds dst_tensor_idx in the expanded layout; FP8
-//     scale sidecars travel beside the hidden payload.
+//     scale sidecars travel beside the hidden payload; a payload is never
+//     dropped silently. Summary and "Direct Recv X design": the sender writes
+//     its rows straight into the receiver's compact recv_x, at the receiver's
+//     exclusive prefix of the per-source counts.
 //   * Issue #647 footer, PR #544 "Fix duplicate calculation of
 //     num_tokens_per_rank": a token counts once per destination rank.
 //
@@ -39,7 +42,11 @@
 //   * FP8: per token and per 128 columns, amax (clamped below at 1e-4),
 //     sf = amax / 448, q = e4m3_rn_satfinite(x * (448 / amax));
 //   * combine: acc = +0; for k in lane order over valid lanes
-//     acc = fma(w_k, y_k, acc); out = bf16_rn(acc).
+//     acc = fma(w_k, y_k, acc); out = bf16_rn(acc);
+//   * compact receive rows: each destination's entries from the start of its
+//     R*M-row window in row-block order; packed: the same order with the
+//     destinations back to back in one buffer of R*T*min(K, R) rows (or a
+//     caller's capacity; entries past it are reported as OVERFLOW).
 //
 // Parity pins for every function here live in the CPU test suite; none is
 // unpinned.
@@ -53,6 +60,7 @@ namespace {
 struct Cfg {
   int32_t n_so, n_su, E, K, T, M, H;
   int32_t x_fp8, recv_fp8, expand, align, compact, zero_padding, sf_pack;
+  int32_t recv_capacity;  // packed receive rows only: rows the receive tensors hold (0 = the bound)
 };
 
 constexpr int kOk = 0;
@@ -180,23 +188,45 @@ int check_cfg(const Cfg& c) {
   if (c.E < R || c.E % R != 0 || c.T > c.M || c.align < 1) return kInvalid;
   if ((c.x_fp8 || c.recv_fp8) && c.H % 128 != 0) return kInvalid;
   if (c.x_fp8 && !c.recv_fp8) return kUnsupported;
+  if (c.compact < 0 || c.compact > 2 || c.recv_capacity < 0) return kInvalid;
   if (c.compact && c.expand) return kUnsupported;
+  if (c.recv_capacity && c.compact != 2) return kUnsupported;
   if (c.zero_padding && !c.expand) return kUnsupported;
   if (c.sf_pack && !c.recv_fp8) return kUnsupported;
   return kOk;
 }
 
-// Receive row of a row-form slot. Row form: the slot itself. Compact (PR #690,
-// Direct Recv X): a destination's entries are packed from row 0 in row-block
-// order, so the entries of row block rb start after everything the
-// destination receives from row blocks before rb (the exclusive prefix of its
-// per-source receive counts).
-int64_t recv_row(const Cfg& c, int d, int64_t slot, const int32_t* recv_psum) {
-  if (!c.compact) return slot;
+// Rows of the receive tensors (recv_x, recv_sf, and the sidecars unless
+// expanded): R regions of R*M rows (row form and compact), or, packed, the
+// capacity (R*T*min(K, R) deduplicated entries at most, or the caller's).
+int64_t entry_rows(const Cfg& c) {
+  const int64_t R = ranks(c);
+  if (c.compact == 2) {
+    if (c.recv_capacity > 0) return c.recv_capacity;
+    return R * c.T * (c.K < R ? c.K : R);
+  }
+  return R * R * c.M;
+}
+
+// Row of a deduplicated (token, destination d) entry with row-form slot
+// `slot` in the receive tensors.
+//   row form:  d*R*M + slot (PR #753, Approach: the slot is already the row).
+//   compact (PR #690, Direct Recv X): destination d's entries are packed from
+//              the start of its R*M-row window in row-block order, so the
+//              entries of row block rb follow everything d receives from row
+//              blocks before rb (the exclusive prefix of its per-source receive
+//              counts): d*R*M + recv_psum[d][rb-1] + slot - rb*M.
+//   packed:    the same, with the destinations back to back instead of one
+//              window each: recv_region[d] = everything destinations before d
+//              receive, in place of d*R*M.
+int64_t entry_row(const Cfg& c, int d, int64_t slot, const int32_t* recv_psum, const int32_t* recv_region) {
   const int R = ranks(c);
+  const int64_t window = static_cast<int64_t>(d) * R * c.M;
+  if (c.compact == 0) return window + slot;
   const int64_t rb = slot / c.M;
   const int64_t before = rb == 0 ? 0 : recv_psum[static_cast<int64_t>(d) * R + rb - 1];
-  return before + (slot - rb * c.M);
+  const int64_t base = c.compact == 1 ? window : recv_region[d];
+  return base + before + (slot - rb * c.M);
 }
 
 // Lane validity: -1 is masked; anything else outside [0, E) is an error; in
@@ -226,7 +256,7 @@ extern "C" {
 
 struct orc_cfg {
   int32_t n_so, n_su, E, K, T, M, H;
-  int32_t x_fp8, recv_fp8, expand, align, compact, zero_padding, sf_pack;
+  int32_t x_fp8, recv_fp8, expand, align, compact, zero_padding, sf_pack, recv_capacity;
 };
 
 static Cfg to_cfg(const orc_cfg* p) {
@@ -268,14 +298,19 @@ void orc_cast_row_fp8_ue8m0(const uint16_t* x, int H, uint8_t* q, uint32_t* word
   cast_row_fp8_ue8m0(x, H, q, words);
 }
 
-// Number of rows the receive buffer needs: R regions of R*M rows (row form),
-// or the expanded upper bound R*T*K + E*(align-1).
+// Number of rows the receive buffer recv_x needs: the expanded upper bound
+// R*T*K + E*(align-1), else the rows of the receive tensors (entry_rows).
 int64_t orc_recv_rows(const orc_cfg* p) {
   const Cfg c = to_cfg(p);
   const int64_t R = ranks(c);
   if (c.expand) return R * c.T * c.K + static_cast<int64_t>(c.E) * (c.align - 1);
-  return R * R * c.M;
+  return entry_rows(c);
 }
+
+// Rows of the sidecar tensors (recv_topk_idx, recv_topk_weights,
+// recv_src_metadata): the deduplicated entries' rows, R*R*M in the row form,
+// compact and expanded layouts, the capacity when packed.
+int64_t orc_sidecar_rows(const orc_cfg* p) { return entry_rows(to_cfg(p)); }
 
 // Dispatch layout: counts, per-lane slots and (expanded) positions.
 //   num_tokens_per_rank   [R][R]    (src, dst): tokens of src that reach dst, once per token
@@ -285,11 +320,13 @@ int64_t orc_recv_rows(const orc_cfg* p) {
 //   recv_cnt              [R][R]    (dst, src) = num_tokens_per_rank transposed
 //   recv_psum             [R][R]    (dst, row block i) inclusive prefix of recv_cnt in
 //                                   row-block order (block i holds source src_of_block(i))
+//   recv_region           [R+1]     (may be null) first packed row of each destination:
+//                                   the entries all destinations before it receive; [R] = total
 //   exp_cnt [R][L], exp_base [R][L+1], exp_region [R+1], exp_pos [R][T][K] (expanded only)
 int orc_layout(const orc_cfg* p, const int64_t* topk_idx, int32_t* num_tokens_per_rank,
                int32_t* num_tokens_per_expert, uint8_t* is_token_in_rank, int32_t* slot_map,
-               int32_t* recv_cnt, int32_t* recv_psum, int32_t* exp_cnt, int32_t* exp_base,
-               int32_t* exp_region, int32_t* exp_pos) {
+               int32_t* recv_cnt, int32_t* recv_psum, int32_t* recv_region, int32_t* exp_cnt,
+               int32_t* exp_base, int32_t* exp_region, int32_t* exp_pos) {
   const Cfg c = to_cfg(p);
   int status = check_cfg(c);
   if (status != kOk) return status;
@@ -334,6 +371,7 @@ int orc_layout(const orc_cfg* p, const int64_t* topk_idx, int32_t* num_tokens_pe
   // receive side: per-source counts and their prefix sums in row-block order
   std::vector<int> src_of_block(R);
   for (int s = 0; s < R; ++s) src_of_block[row_block(c, s)] = s;
+  int32_t all = 0;
   for (int d = 0; d < R; ++d) {
     int32_t acc = 0;
     for (int s = 0; s < R; ++s) recv_cnt[d * R + s] = num_tokens_per_rank[s * R + d];
@@ -341,7 +379,10 @@ int orc_layout(const orc_cfg* p, const int64_t* topk_idx, int32_t* num_tokens_pe
       acc += recv_cnt[d * R + src_of_block[i]];
       recv_psum[d * R + i] = acc;
     }
+    if (recv_region) recv_region[d] = all;
+    all += acc;
   }
+  if (recv_region) recv_region[R] = all;
 
   if (c.expand) {
     // per (destination, local expert) totals, aligned block starts, regions
@@ -381,20 +422,22 @@ int orc_layout(const orc_cfg* p, const int64_t* topk_idx, int32_t* num_tokens_pe
 }
 
 // The receive rows of one source token (s, t), computed from that token's
-// inputs and its layout entries.
+// inputs and its layout entries (recv_psum for the compact and packed layouts,
+// recv_region for the packed one, exp_region when expanded).
 //   hid      : the row as received (H bf16 values, or H e4m3 codes)
 //   hid_sf   : its scale sidecar (FP8 receive only): G = H/128 fp32 scales, or
 //              ceil(G/4) words of packed exponent bytes
-//   hid_dst / hid_row : the n_hid (destination, row) pairs that receive the
-//              hidden row; row = slot (row form), its compact row, or the
-//              expanded position inside the destination's region
-//   meta_dst / meta_row : the n_meta deduplicated (destination, row) pairs
+//   hid_dst / hid_row : the n_hid (destination, row of recv_x) pairs that
+//              receive the hidden row: the entry's row (entry_row), or the
+//              expanded row exp_region[d] + position
+//   meta_dst / meta_row : the n_meta deduplicated entries: destination and row
+//              of the sidecar tensors (entry_row)
 //   meta_idx [K][K] int64, meta_w [K][K] fp32, meta_md [K][2+K] int32: the
-//              sidecar rows written at (meta_dst[i], meta_row[i])
+//              sidecar rows written at meta_row[i]
 // Returns n_hid | (n_meta << 8).
 int orc_dispatch_token(const orc_cfg* p, int s, int t, const int32_t* slot_tok,
-                       const int32_t* pos_tok, const int32_t* recv_psum, const void* x_row,
-                       const float* x_sf_row,
+                       const int32_t* pos_tok, const int32_t* recv_psum, const int32_t* recv_region,
+                       const int32_t* exp_region, const void* x_row, const float* x_sf_row,
                        const int64_t* idx_tok, const float* w_tok, uint8_t* hid, float* hid_sf,
                        int32_t* hid_dst, int64_t* hid_row, int32_t* meta_dst, int64_t* meta_row,
                        int64_t* meta_idx, float* meta_w, int32_t* meta_md) {
@@ -428,11 +471,11 @@ int orc_dispatch_token(const orc_cfg* p, int s, int t, const int32_t* slot_tok,
       if (lane_d[j] == d && slot_tok[j] >= 0) first = false;
     if (c.expand) {
       hid_dst[n_hid] = d;
-      hid_row[n_hid] = pos_tok[k];
+      hid_row[n_hid] = static_cast<int64_t>(exp_region[d]) + pos_tok[k];
       ++n_hid;
     }
     if (!first) continue;
-    const int64_t row = recv_row(c, d, slot_tok[k], recv_psum);
+    const int64_t row = entry_row(c, d, slot_tok[k], recv_psum, recv_region);
     if (!c.expand) {
       hid_dst[n_hid] = d;
       hid_row[n_hid] = row;
@@ -455,16 +498,16 @@ int orc_dispatch_token(const orc_cfg* p, int s, int t, const int32_t* slot_tok,
 }
 
 // Full dispatch into caller-provided receive buffers (only filled rows are
-// written; the rest are left as they are). recv_psum is needed for the
-// compact layout only.
-//   recv_x [recv_rows][H] (bf16 or e4m3); recv_sf [recv_rows][sf words] (FP8 only)
-//   recv_topk_idx [R][R*M][K], recv_topk_weights [R][R*M][K],
-//   recv_src_metadata [R][R*M][2+K]
-// In the row form, destination d's rows start at d*R*M; expanded rows at
-// exp_region[d].
+// written; the rest are left as they are).
+//   recv_x [orc_recv_rows][H] (bf16 or e4m3); recv_sf [orc_recv_rows][sf words] (FP8 only)
+//   recv_topk_idx [orc_sidecar_rows][K], recv_topk_weights [orc_sidecar_rows][K],
+//   recv_src_metadata [orc_sidecar_rows][2+K]
+// recv_psum is needed for the compact and packed layouts, recv_region for the
+// packed one. An entry whose packed row is past the capacity is not written and
+// the result is OVERFLOW (never dropped silently).
 int orc_dispatch(const orc_cfg* p, const int32_t* slot_map, const int32_t* exp_pos,
                  const int32_t* exp_region, const int32_t* exp_cnt, const int32_t* exp_base,
-                 const int32_t* recv_psum, const void* x, const float* x_sf,
+                 const int32_t* recv_psum, const int32_t* recv_region, const void* x, const float* x_sf,
                  const int64_t* topk_idx, const float* topk_weights, void* recv_x,
                  float* recv_sf, int64_t* recv_topk_idx, float* recv_topk_weights,
                  int32_t* recv_src_metadata) {
@@ -472,7 +515,7 @@ int orc_dispatch(const orc_cfg* p, const int32_t* slot_map, const int32_t* exp_p
   int status = check_cfg(c);
   if (status != kOk) return status;
   const int R = ranks(c), K = c.K, T = c.T, H = c.H, G = H / 128, SW = sf_words(H, c.sf_pack);
-  const int64_t region_rows = static_cast<int64_t>(R) * c.M;
+  const int64_t cap = entry_rows(c);
   const size_t in_eb = c.x_fp8 ? 1 : 2, out_eb = c.recv_fp8 ? 1 : 2;
 
   std::vector<uint8_t> hid(static_cast<size_t>(H) * 2);
@@ -486,20 +529,24 @@ int orc_dispatch(const orc_cfg* p, const int32_t* slot_map, const int32_t* exp_p
       const int64_t tok = static_cast<int64_t>(s) * T + t;
       for (int k = 0; k < K; ++k) lane_valid(c, topk_idx + tok * K, k, &status);
       const int n = orc_dispatch_token(
-          p, s, t, slot_map + tok * K, c.expand ? exp_pos + tok * K : nullptr, recv_psum,
-          static_cast<const uint8_t*>(x) + tok * H * in_eb, x_sf ? x_sf + tok * SW : nullptr,
+          p, s, t, slot_map + tok * K, c.expand ? exp_pos + tok * K : nullptr, recv_psum, recv_region,
+          exp_region, static_cast<const uint8_t*>(x) + tok * H * in_eb, x_sf ? x_sf + tok * SW : nullptr,
           topk_idx + tok * K, topk_weights + tok * K, hid.data(), hid_sf.data(), hid_dst.data(),
           hid_row.data(), meta_dst.data(), meta_row.data(), meta_idx.data(), meta_w.data(),
           meta_md.data());
       const int n_hid = n & 0xFF, n_meta = n >> 8;
       for (int i = 0; i < n_hid; ++i) {
-        const int64_t row = c.expand ? exp_region[hid_dst[i]] + hid_row[i]
-                                     : hid_dst[i] * region_rows + hid_row[i];
+        const int64_t row = hid_row[i];
+        if (c.compact == 2 && row >= cap) {
+          status = kOverflow;
+          continue;
+        }
         std::memcpy(static_cast<uint8_t*>(recv_x) + row * H * out_eb, hid.data(), H * out_eb);
         if (c.recv_fp8) std::memcpy(recv_sf + row * SW, hid_sf.data(), sizeof(float) * SW);
       }
       for (int i = 0; i < n_meta; ++i) {
-        const int64_t row = meta_dst[i] * region_rows + meta_row[i];
+        const int64_t row = meta_row[i];
+        if (c.compact == 2 && row >= cap) continue;  // reported with the hidden row
         if (recv_topk_idx) std::memcpy(recv_topk_idx + row * K, &meta_idx[i * K], 8 * K);
         if (recv_topk_weights) std::memcpy(recv_topk_weights + row * K, &meta_w[i * K], 4 * K);
         if (recv_src_metadata)
@@ -522,6 +569,39 @@ int orc_dispatch(const orc_cfg* p, const int32_t* slot_map, const int32_t* exp_p
         }
       }
     }
+  }
+  return status;
+}
+
+// Row of every top-k lane in the receive tensors, from the layout:
+//   hid_rows [R][T][K]  the recv_x row lane k's expert reads: its deduplicated
+//                       entry's row (entry_row), or, expanded, exp_region[d] +
+//                       its position;
+//   side_rows [R][T][K] the sidecar row of its deduplicated entry (entry_row);
+// both -1 for a masked or invalid lane and, packed, for an entry past the
+// capacity (OVERFLOW is returned then).
+int orc_lane_rows(const orc_cfg* p, const int64_t* topk_idx, const int32_t* slot_map,
+                  const int32_t* exp_pos, const int32_t* exp_region, const int32_t* recv_psum,
+                  const int32_t* recv_region, int64_t* hid_rows, int64_t* side_rows) {
+  const Cfg c = to_cfg(p);
+  int status = check_cfg(c);
+  if (status != kOk) return status;
+  const int R = ranks(c), L = c.E / R, K = c.K;
+  const int64_t cap = entry_rows(c);
+  const int64_t lanes = static_cast<int64_t>(R) * c.T * K;
+  for (int64_t i = 0; i < lanes; ++i) {
+    const int64_t* idx_tok = topk_idx + i / K * K;
+    hid_rows[i] = -1;
+    side_rows[i] = -1;
+    if (!lane_valid(c, idx_tok, static_cast<int>(i % K), &status) || slot_map[i] < 0) continue;
+    const int d = static_cast<int>(topk_idx[i]) / L;
+    const int64_t row = entry_row(c, d, slot_map[i], recv_psum, recv_region);
+    if (c.compact == 2 && row >= cap) {
+      status = kOverflow;
+      continue;
+    }
+    side_rows[i] = row;
+    hid_rows[i] = c.expand ? (exp_pos[i] < 0 ? -1 : static_cast<int64_t>(exp_region[d]) + exp_pos[i]) : row;
   }
   return status;
 }
@@ -552,16 +632,18 @@ void orc_combine_gathered(int K, int H, int64_t n, const int64_t* lane_rows, con
   }
 }
 
-// Full combine: y holds the expert outputs in the receive layout (row form or
-// compact: destination d's rows start at d*R*M; expanded: at exp_region[d]).
+// Full combine: y holds the expert outputs in the receive layout (the rows
+// of recv_x: entry_row of each lane's deduplicated entry, or exp_region[d] +
+// position when expanded). A lane whose packed row is past the capacity was
+// never received: it is left out of the sum and the result is OVERFLOW.
 int orc_combine(const orc_cfg* p, const int32_t* slot_map, const int32_t* exp_pos,
-                const int32_t* exp_region, const int32_t* recv_psum, const uint16_t* y, const int64_t* topk_idx,
-                const float* topk_weights, uint16_t* out) {
+                const int32_t* exp_region, const int32_t* recv_psum, const int32_t* recv_region,
+                const uint16_t* y, const int64_t* topk_idx, const float* topk_weights, uint16_t* out) {
   const Cfg c = to_cfg(p);
   int status = check_cfg(c);
   if (status != kOk) return status;
   const int R = ranks(c), L = c.E / R, K = c.K, T = c.T, H = c.H;
-  const int64_t region_rows = static_cast<int64_t>(R) * c.M;
+  const int64_t cap = entry_rows(c);
   std::vector<const uint16_t*> rows(K);
   for (int s = 0; s < R; ++s) {
     for (int t = 0; t < T; ++t) {
@@ -572,7 +654,11 @@ int orc_combine(const orc_cfg* p, const int32_t* slot_map, const int32_t* exp_po
         const int d = static_cast<int>(topk_idx[tok * K + k]) / L;
         if ((c.expand ? exp_pos[tok * K + k] : slot_map[tok * K + k]) < 0) continue;
         const int64_t r = c.expand ? static_cast<int64_t>(exp_region[d]) + exp_pos[tok * K + k]
-                                   : d * region_rows + recv_row(c, d, slot_map[tok * K + k], recv_psum);
+                                   : entry_row(c, d, slot_map[tok * K + k], recv_psum, recv_region);
+        if (c.compact == 2 && r >= cap) {
+          status = kOverflow;
+          continue;
+        }
         rows[k] = y + r * H;
       }
       orc_combine_token(K, H, rows.data(), topk_weights + tok * K, out + tok * H);

@@ -80,18 +80,9 @@ def assert_layout_equal(got, exp, expand):
 
 
 def filled_rows(wl, olay, idx):
-    """(hidden rows, sidecar rows) the oracle fills: global row indices."""
-    rows = oracle.global_rows(wl, olay, idx)
-    R, M = wl.num_ranks, wl.num_max_tokens_per_rank
-    hid = np.unique(rows[rows >= 0])
-    L = wl.num_experts // R
-    idx = idx.numpy() if hasattr(idx, "numpy") else idx
-    d = np.where(idx >= 0, idx // L, 0)
-    slot = olay["slot_map"].astype(np.int64)
-    row = oracle.recv_rows_of_slots(wl, olay, d, np.maximum(slot, 0))
-    side = np.where(slot >= 0, d * R * M + row, -1)
-    side = np.unique(side[side >= 0])
-    return hid, side
+    """(recv_x rows, sidecar rows) the oracle fills: its lane rows, deduplicated."""
+    st, hid, side = oracle.lane_rows(wl, olay, idx)
+    return np.unique(hid[hid >= 0]), np.unique(side[side >= 0])
 
 
 def compare_dispatch(run: GpuRun, olay, orec):
@@ -105,10 +96,10 @@ def compare_dispatch(run: GpuRun, olay, orec):
     if wl.recv_dtype == "fp8":
         got_sf = run.recv.recv_sf.index_select(0, hid_t).cpu().numpy()
         assert np.array_equal(got_sf.view(np.uint32), orec["recv_sf"][hid].view(np.uint32)), "recv_sf differs"
-    R, M, K = wl.num_ranks, wl.num_max_tokens_per_rank, wl.num_topk
+    K = wl.num_topk
     for name, width in (("recv_topk_idx", K), ("recv_topk_weights", K), ("recv_src_metadata", K + 2)):
-        g = getattr(run.recv, name).reshape(R * R * M, width).index_select(0, side_t).cpu().numpy()
-        e = orec[name].reshape(R * R * M, width)[side]
+        g = getattr(run.recv, name).reshape(-1, width).index_select(0, side_t).cpu().numpy()
+        e = orec[name][side]
         assert np.array_equal(g.view(np.uint8), e.view(np.uint8)), f"{name} differs"
     return hid, side
 

@@ -47,7 +47,7 @@ def test_algorithmic_bytes_equal_what_the_oracle_moves(name):
     rx = np.ascontiguousarray(rec["recv_x"]).view(np.uint8).reshape(rec["recv_x"].shape[0], -1)
     written = int((rx != 0xFF).any(axis=1).sum())
     md = rec["recv_src_metadata"].reshape(-1, K + 2)
-    side_rows = int((md != 0).any(axis=1).sum())  # a written row carries -1 or a position past field 1
+    side_rows = int((md[:, 0] != -1).sum())  # a written row carries its source rank (>= 0) in field 0
     ix = idx.numpy()
     tokens_with_lane = int((ix >= 0).any(axis=-1).sum())
     rows = oracle.global_rows(wl, lay, idx)

@@ -22,7 +22,7 @@ import torch
 import combine_ep_get_02_gb300 as ep
 import oracle
 import workloads as W
-from _harness import assert_layout_equal, filled_rows, u16
+from _harness import assert_layout_equal, u16
 
 pytestmark = pytest.mark.gpu
 
@@ -119,13 +119,11 @@ def test_every_routing_matches_the_oracle(name, copy_path):
         if wl.recv_dtype == "fp8":
             assert np.array_equal(recv.recv_sf[:rows].cpu().numpy().view(np.uint32),
                                   orec["recv_sf"][:rows].view(np.uint32)), (name, c)
-        filled = filled_rows(wl, olay, idx)[1]
-        untouched = np.setdiff1d(np.arange(R * R * M), filled)
+        # whole sidecar buffers: written rows equal, the rest still 0xFF on both sides
         for key, width in side_tensors:
-            gs = getattr(recv, key).reshape(R * R * M, width).cpu().numpy().view(np.uint8)
-            es = orec[key].reshape(R * R * M, width).view(np.uint8)
-            assert np.array_equal(gs[filled], es[filled]), (name, c, key)
-            assert np.all(gs[untouched] == 0xFF), (name, c, key)
+            gs = getattr(recv, key).reshape(-1, width).cpu().numpy().view(np.uint8)
+            es = orec[key].view(np.uint8)
+            assert np.array_equal(gs, es), (name, c, key)
 
         exp = oracle.combine_gathered(oracle.global_rows(wl, olay, idx).reshape(-1, K), y_h,
                                       w.numpy().reshape(-1, K))

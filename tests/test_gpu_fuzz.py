@@ -15,7 +15,7 @@ import torch
 import combine_ep_get_02_gb300 as ep
 import oracle
 import workloads as W
-from _harness import GpuRun, assert_layout_equal, filled_rows, inputs, u16
+from _harness import GpuRun, assert_layout_equal, inputs, u16
 
 pytestmark = pytest.mark.gpu
 
@@ -80,15 +80,11 @@ def test_fuzz_case(seed):
     if wl.recv_dtype == "fp8":
         got_sf = run.recv.recv_sf[:rows].cpu().numpy().view(np.uint32)
         assert np.array_equal(got_sf, orec["recv_sf"][:rows].view(np.uint32)), wl
-    # sidecars: compare the rows the oracle writes (others are 0xFF on the GPU and 0 in the oracle)
-    R, M, K = wl.num_ranks, wl.num_max_tokens_per_rank, wl.num_topk
-    filled = filled_rows(wl, olay, idx)[1]
+    # whole sidecar buffers: written rows equal, the rest still 0xFF on both sides
+    K = wl.num_topk
     for name, width in (("recv_topk_idx", K), ("recv_topk_weights", K), ("recv_src_metadata", K + 2)):
-        g = getattr(run.recv, name).reshape(R * R * M, width).cpu().numpy()
-        e = orec[name].reshape(R * R * M, width)
-        assert np.array_equal(g[filled].view(np.uint8), e[filled].view(np.uint8)), (wl, name)
-        untouched = np.setdiff1d(np.arange(R * R * M), filled)
-        assert np.all(g[untouched].view(np.uint8) == 0xFF), (wl, name)
+        g = getattr(run.recv, name).reshape(-1, width).cpu().numpy()
+        assert np.array_equal(g.view(np.uint8), orec[name].view(np.uint8)), (wl, name)
 
     exp = oracle.combine_gathered(oracle.global_rows(wl, olay, idx).reshape(-1, K),
                                   u16(y), w.numpy().reshape(-1, K)) if wl.num_tokens else None

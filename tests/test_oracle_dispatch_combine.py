@@ -68,9 +68,9 @@ def test_bf16_rows_are_the_source_rows(orc, name):
         assert np.array_equal(rec["recv_x"][g], xb[s, t])
         # sidecars: destination-local expert index / weight on lanes to d, else -1 / 0
         on = (idx[s, t] >= 0) & (idx[s, t] // L == d)
-        assert rec["recv_topk_idx"][d, row].tolist() == np.where(on, idx[s, t] - d * L, -1).tolist()
-        assert rec["recv_topk_weights"][d, row].tolist() == np.where(on, w[s, t], 0.0).astype(np.float32).tolist()
-        assert rec["recv_src_metadata"][d, row].tolist() == [s, t] + [-1] * K
+        assert rec["recv_topk_idx"][g].tolist() == np.where(on, idx[s, t] - d * L, -1).tolist()
+        assert rec["recv_topk_weights"][g].tolist() == np.where(on, w[s, t], 0.0).astype(np.float32).tolist()
+        assert rec["recv_src_metadata"][g].tolist() == [s, t] + [-1] * K
     assert not rec["recv_x"][~filled].any()
     assert filled.sum() == lay["num_tokens_per_rank"].sum()
 
@@ -134,7 +134,7 @@ def test_expanded_rows_and_metadata(orc):
     assert n == int(lay["exp_cnt"].sum())
     for s, t, d, row in dedup_entries(wl, idx, lay["slot_map"]):
         on = (idx[s, t] >= 0) & (idx[s, t] // L == d)
-        assert rec["recv_src_metadata"][d, row].tolist() == [s, t] + np.where(on, pos[s, t], -1).tolist()
+        assert rec["recv_src_metadata"][d * R * M + row].tolist() == [s, t] + np.where(on, pos[s, t], -1).tolist()
 
 
 # ---- combine -------------------------------------------------------------
@@ -227,26 +227,34 @@ def _row_block(wl, s):
     return s if wl.n_so == 1 else (s % wl.n_su) * wl.n_so + s // wl.n_su
 
 
+@pytest.mark.parametrize("mode", [1, 2])
 @pytest.mark.parametrize("name", ["direct_zipf_compact", "hybrid_compact"])
-def test_compact_rows_pack_each_destination_in_row_block_order(orc, name):
+def test_compact_rows_pack_each_destination_in_row_block_order(orc, name, mode):
     """Each destination's entries, sorted by (source row block, token), occupy
-    rows 0, 1, 2, ... of its region: the compact receive layout."""
-    wl = W.PARITY[name].replace(num_tokens=23, num_max_tokens_per_rank=29, hidden=128)
+    consecutive rows: from the start of the destination's R*M-row window
+    (compact, PR #690 Direct Recv X), or right after everything the
+    destinations before it receive (packed: destinations back to back)."""
+    wl = W.PARITY[name].replace(num_tokens=23, num_max_tokens_per_rank=29, hidden=128, compact=mode)
     idx, w = W.routing(wl)
     x, _ = W.hidden(wl)
     st, lay = orc.layout(wl, idx)
     assert st == 0
-    R, T, K = wl.num_ranks, wl.num_tokens, wl.num_topk
+    R, T, K, M = wl.num_ranks, wl.num_tokens, wl.num_topk, wl.num_max_tokens_per_rank
     L = wl.num_experts // R
     idx_np = idx.numpy()
     xb = _bits(x)
     expect = {}
+    base = 0
     for d in range(R):
         ents = sorted({(_row_block(wl, s), t, s) for s in range(R) for t in range(T)
                        for e in idx_np[s, t] if e >= 0 and e // L == d})
+        start = d * R * M if mode == 1 else base
         for i, (_, t, s) in enumerate(ents):
-            expect[(s, t, d)] = i
+            expect[(s, t, d)] = start + i
         assert len(ents) == lay["recv_cnt"][d].sum()
+        assert lay["recv_region"][d] == base
+        base += len(ents)
+    assert lay["recv_region"][R] == base
     got = {}
     for s in range(R):
         for t in range(T):
@@ -256,30 +264,77 @@ def test_compact_rows_pack_each_destination_in_row_block_order(orc, name):
             assert sorted(zip(o["hid_dst"].tolist(), o["hid_row"].tolist())) == \
                 sorted(zip(o["meta_dst"].tolist(), o["meta_row"].tolist()))
     assert got == expect
+    if mode == 2:
+        # the packed buffer holds R*T*min(K, R) rows: every token has at most
+        # min(K, R) distinct destinations
+        assert orc.recv_rows(wl) == R * T * min(K, R) >= base
 
 
 @pytest.mark.parametrize("name", ["direct_zipf_compact", "hybrid_compact"])
-def test_compact_and_row_form_give_the_same_combine(orc, name):
+def test_compact_packed_and_row_form_give_the_same_combine(orc, name):
     wl = W.PARITY[name].replace(num_tokens=40, num_max_tokens_per_rank=48, hidden=256)
     idx, w = W.routing(wl)
     x, _ = W.hidden(wl)
     outs = []
-    for compact in (True, False):
-        v = wl.replace(compact=compact)
+    R, M, K = wl.num_ranks, wl.num_max_tokens_per_rank, wl.num_topk
+    for mode in (0, 1, 2):
+        v = wl.replace(compact=mode)
         _, lay = orc.layout(v, idx)
         st, rec = orc.dispatch(v, lay, x, None, idx, w)
         assert st == 0
         st, out = orc.combine(v, lay, rec["recv_x"], idx, w)
         assert st == 0
         outs.append(out)
-        if compact:
-            # filled rows of destination d are exactly the first sum_s recv_cnt[d][s]
-            R, M = v.num_ranks, v.num_max_tokens_per_rank
-            md = rec["recv_src_metadata"].reshape(R, R * M, -1)
+        md = rec["recv_src_metadata"]
+        if mode == 1:
+            # filled rows of destination d are exactly the first sum_s recv_cnt[d][s] of its window
+            md = md.reshape(R, R * M, -1)
             for d in range(R):
                 n = int(lay["recv_cnt"][d].sum())
                 assert np.all(md[d, :n, 0] >= 0) and not md[d, n:].any()
-    assert np.array_equal(outs[0], outs[1])
+        if mode == 2:
+            # packed: the first recv_region[R] rows are filled, destination by destination
+            n = int(lay["recv_region"][R])
+            assert md.shape == (R * wl.num_tokens * min(K, R), K + 2)
+            assert np.all(md[:n, 0] >= 0) and not md[n:].any()
+            for d in range(R):
+                a, b = lay["recv_region"][d], lay["recv_region"][d + 1]
+                assert np.all(rec["recv_topk_idx"][a:b].max(-1) >= 0)  # a lane of d on every row
+                assert b - a == lay["recv_cnt"][d].sum()
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+
+
+def test_packed_capacity_overflow_is_reported_not_silent(orc):
+    """Packed rows past a caller's capacity are not written and the call
+    reports OVERFLOW (PR #690 review: a payload is never dropped silently); the
+    rows below the capacity are those of the full-capacity dispatch, and
+    combine leaves the lanes it cannot read out of the sum, reporting it."""
+    wl = W.PARITY["hybrid_packed"].replace(num_tokens=20, num_max_tokens_per_rank=20, hidden=128)
+    idx, w = W.routing(wl)
+    x, _ = W.hidden(wl)
+    _, lay = orc.layout(wl, idx)
+    total = int(lay["recv_region"][-1])
+    st, full = orc.dispatch(wl, lay, x, None, idx, w, fill=0xAB)
+    assert st == 0
+    cap = total - 7
+    small_wl = wl.replace(recv_capacity=cap)
+    assert orc.recv_rows(small_wl) == cap and orc.sidecar_rows(small_wl) == cap
+    st, part = orc.dispatch(small_wl, lay, x, None, idx, w, fill=0xAB)
+    assert st == orc.OVERFLOW
+    for k in ("recv_x", "recv_topk_idx", "recv_topk_weights", "recv_src_metadata"):
+        assert np.array_equal(part[k], full[k][:cap]), k
+    st, hid, side = orc.lane_rows(small_wl, lay, idx)
+    assert st == orc.OVERFLOW
+    st0, hid0, _ = orc.lane_rows(wl, lay, idx)
+    assert st0 == 0 and np.array_equal(hid, np.where(hid0 < cap, hid0, -1))
+    y = np.arange(total * wl.hidden, dtype=np.uint32).reshape(total, wl.hidden).astype(np.uint16) & 0x3FFF
+    st, out_full = orc.combine(wl.replace(recv_capacity=total), lay, y, idx, w)
+    assert st == 0
+    st, out_part = orc.combine(small_wl, lay, y[:cap], idx, w)
+    assert st == orc.OVERFLOW
+    lost = (hid0 >= cap).any(-1)  # tokens with a lane past the capacity
+    assert lost.any() and np.array_equal(out_part[~lost], out_full[~lost])
+    assert orc.combine(wl.replace(recv_capacity=3), lay, y, idx, w)[0] == orc.OVERFLOW
 
 
 def test_zero_padding_of_aligned_expanded_blocks(orc):

@@ -46,7 +46,10 @@ class Workload:
     recv_dtype: str = "bf16"      # "bf16" | "fp8" (fused cast when x is bf16)
     expand: bool = False
     expert_alignment: int = 1
-    compact: bool = False         # compact receive rows (row form only)
+    compact: int = 0              # receive rows (row form only): 0 at their slots; 1 compact,
+                                  # packed from the start of each destination's window; 2 packed,
+                                  # destinations back to back
+    recv_capacity: int = 0        # packed receive rows: rows of the receive tensors (0 = the bound)
     zero_padding: bool = False    # zero the alignment padding rows (expanded only)
     sf_pack: bool = False         # packed power-of-two scales, 4 per 32-bit word
     routing: str = "gauss"        # "gauss" | "zipf" | "hot"
@@ -100,9 +103,16 @@ PARITY = {
     "expanded": WORKLOADS["expanded"].replace(num_tokens=100, num_max_tokens_per_rank=100),
     # compact receive rows (each destination's rows packed from row 0)
     "direct_zipf_compact": WORKLOADS["direct_zipf"].replace(
-        name="direct_zipf_compact", compact=True, num_tokens=300, num_max_tokens_per_rank=320),
+        name="direct_zipf_compact", compact=1, num_tokens=300, num_max_tokens_per_rank=320),
     "hybrid_compact": WORKLOADS["hybrid_rowform"].replace(
-        name="hybrid_compact", compact=True, num_tokens=300, num_max_tokens_per_rank=300),
+        name="hybrid_compact", compact=1, num_tokens=300, num_max_tokens_per_rank=300),
+    # packed receive rows (destinations back to back in a buffer of R*T*min(K,R) rows)
+    "direct_zipf_packed": WORKLOADS["direct_zipf"].replace(
+        name="direct_zipf_packed", compact=2, num_tokens=300, num_max_tokens_per_rank=320),
+    "hybrid_packed": WORKLOADS["hybrid_rowform"].replace(
+        name="hybrid_packed", compact=2, num_tokens=300, num_max_tokens_per_rank=300),
+    "dsv3_fp8_packed_rows": WORKLOADS["dsv3_fp8"].replace(
+        name="dsv3_fp8_packed_rows", compact=2, num_tokens=288, num_max_tokens_per_rank=288),
     # packed power-of-two scales (fused cast, and pre-cast input carrying them)
     "dsv3_fp8_packed": WORKLOADS["dsv3_fp8"].replace(
         name="dsv3_fp8_packed", sf_pack=True, num_tokens=288, num_max_tokens_per_rank=288),
