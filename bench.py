@@ -41,6 +41,7 @@ import workloads as W  # noqa: E402
 METRIC = "dispatch+combine tokens/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
 DEFAULT_WORKLOAD = "dsv3_fp8"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0  # GB300's nominal HBM3e bandwidth: context beside the measured copy peak
 
 
 def parse():
@@ -53,7 +54,9 @@ def parse():
     p.add_argument("--tokens", type=int, default=0,
                    help="override tokens per rank (small cases for profiling only)")
     p.add_argument("--compact", action="store_true",
-                   help="compact receive rows (each destination packed from row 0)")
+                   help="packed receive rows: destinations back to back in R*T*min(K,R) rows")
+    p.add_argument("--compact-window", action="store_true",
+                   help="compact receive rows inside each destination's R*M-row window")
     p.add_argument("--align", type=int, default=0, help="expert_alignment of the expanded layout")
     p.add_argument("--zero-padding", action="store_true", help="zero the alignment padding rows")
     p.add_argument("--sf-pack", action="store_true",
@@ -82,7 +85,9 @@ def workload(args):
     if args.tokens:
         wl = wl.replace(num_tokens=args.tokens, num_max_tokens_per_rank=max(args.tokens, 1))
     if args.compact:
-        wl = wl.replace(compact=True)
+        wl = wl.replace(compact=2)
+    elif args.compact_window:
+        wl = wl.replace(compact=1)
     if args.align:
         wl = wl.replace(expert_alignment=args.align)
     if args.zero_padding:
@@ -114,8 +119,10 @@ def host_cpu() -> str:
 def describe(wl) -> str:
     lay = "expanded per-expert blocks" if wl.expand else (
         f"hybrid row form {wl.n_so}x{wl.n_su}" if wl.n_so > 1 else "direct row form")
-    if wl.compact:
-        lay += ", compact receive rows"
+    if wl.compact == 1:
+        lay += ", compact receive rows (per-destination windows)"
+    elif wl.compact == 2:
+        lay += ", packed receive rows (destinations back to back)"
     if wl.expand and wl.expert_alignment > 1:
         lay += f", blocks aligned to {wl.expert_alignment}" + (" with zeroed padding" if wl.zero_padding else "")
     cast = {("bf16", "fp8"): "bf16 x cast to fp8-e4m3 inside dispatch (" + (
@@ -164,6 +171,25 @@ def algorithmic_bytes(wl, ntpr, valid_lanes, tokens_with_lane, pad_rows=0):
                + n_tok * H * 2                                     # out written
                + n_tok * K * (8 + 4 + 4))
     return {"layout": layout, "dispatch": dispatch, "combine": combine, "dispatch_read": dispatch_read}
+
+
+def run_config(wl, args, world, ntpr):
+    """The `config` object of the JSON line; both arms print the same one."""
+    return {"workload": describe(wl) + (" (cached: layout replayed, not timed)" if args.cached else ""),
+            "tokens_per_step": wl.num_ranks * wl.num_tokens, "dedup_rows": ntpr,
+            "l2": "inputs larger than L2 between steps (no flush)",
+            "copy_path": {0: "automatic", 1: "register copies", 2: "bulk copies"}[args.copy_path],
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
+def receive_bytes(recv, y, identity):
+    """Device bytes of the receive tensors (and of the expert outputs y when they
+    are a separate buffer): what the receive layout costs in memory."""
+    n = sum(t.numel() * t.element_size() for t in (recv.recv_x, recv.recv_sf, recv.recv_topk_idx,
+                                                     recv.recv_topk_weights, recv.recv_src_metadata)
+            if t is not None)
+    return {"recv_buffer_bytes": n, "recv_x_rows": recv.recv_x.shape[0],
+            "expert_output_bytes": 0 if identity else y.numel() * y.element_size()}
 
 
 # ---- clocks ----------------------------------------------------------------
@@ -362,17 +388,16 @@ def native(args):
                   if wl.recv_dtype == "fp8" and wl.x_dtype == "bf16" else
                   f"{wl.x_dtype} x -> {wl.recv_dtype} recv, fp32 combine accumulate"),
         "data": "synthetic (seeded routing and activations)",
-        "config": {"workload": describe(wl) + (" (cached: layout replayed, not timed)" if args.cached else ""),
-                   "tokens_per_step": R * T, "dedup_rows": ntpr,
-                   "l2": "inputs larger than L2 between steps (no flush)",
-                   "copy_path": {0: "automatic", 1: "register copies", 2: "bulk copies"}[args.copy_path],
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "config": run_config(wl, args, world, ntpr),
+        "memory": receive_bytes(recv, y, identity),
         "phases": {
             k: {"us": phase_ms[k] * 1e3, "us_median": phase_med[k] * 1e3, "algorithmic_bytes": abytes[k],
-                "gbs": gbs[k], "frac_of_peak": gbs[k] / peak} for k in ("layout", "dispatch", "combine")},
+                "gbs": gbs[k], "frac_of_peak": gbs[k] / peak, "frac_of_nominal": gbs[k] / NOMINAL_HBM_GBS}
+            for k in ("layout", "dispatch", "combine")},
         "roofline": {"kernel": f"{dominant}_kernel", "bound": "hbm", "achieved": gbs[dominant],
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": gbs[dominant] / peak, "traffic": ncu_traffic(f"{dominant}_kernel", wl, R * T)},
+                     "frac": gbs[dominant] / peak, "traffic": ncu_traffic(f"{dominant}_kernel", wl, R * T),
+                     "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": gbs[dominant] / NOMINAL_HBM_GBS},
         "clocks": clocks.summary(),
         "gpu_launches": args.steps * launches_per_step(wl, args.cached),
     }
@@ -656,7 +681,15 @@ def cpu_baseline(wl, idx_h, w_h, x_h, sf_h, y_dev, seconds):
                        f"single-threaded C++ oracle, scaled to tokens/s")}
 
 
+REF_TOKENS_PER_STEP = 1024
+
+
 def reference(args):
+    """The oracle, as it stands, timed on the host's cores. A step is a bounded
+    sample of the workload: the layout of every token plus dispatch and combine
+    of REF_TOKENS_PER_STEP seeded random source tokens; `ms_per_step` is the
+    measured time of that sampled work, and `value` extrapolates it to the whole
+    workload (tokens/s of the full job at the sampled per-token cost)."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -665,11 +698,10 @@ def reference(args):
     idx_h, w_h = W.routing(wl)
     x_h, sf_h = W.hidden(wl)
     R, T = wl.num_ranks, wl.num_tokens
-    # expert outputs for the sampled tokens: drawn on the host for the rows they read
     import oracle
-    st, olay = oracle.layout(wl, idx_h)
-    rows = oracle.global_rows(wl, olay, idx_h)
-    n_rows = int(rows.max()) + 1 if rows.size and rows.max() >= 0 else 1
+    st, olay = oracle.layout(wl, idx_h)  # the config's dedup row count (not timed)
+    ntpr = int(olay["num_tokens_per_rank"].sum())
+    # expert outputs for the sampled tokens: drawn on the host for the rows they read
     gen = torch.Generator().manual_seed(wl.seed * 1_000_003 + 1)
 
     class _LazyRows:  # y rows on demand: same shape of access as a device buffer
@@ -678,23 +710,25 @@ def reference(args):
         def index_select(self, dim, ix):
             return torch.randn(ix.numel(), wl.hidden, generator=gen).to(torch.bfloat16)
 
-    per_step_tokens = 256
-    times = []
+    n_tok = min(REF_TOKENS_PER_STEP, R * T)
+    step_s, per_token = [], []
     for i in range(args.warmup + args.steps):
-        per, n, *_ = cpu_sample(wl, idx_h, w_h, x_h, sf_h, _LazyRows(), per_step_tokens, seed=i)
+        per, n, t_layout, t_disp, t_comb = cpu_sample(wl, idx_h, w_h, x_h, sf_h, _LazyRows(), n_tok, seed=i)
         if i >= args.warmup:
-            times.append(per)
-    per = statistics.mean(times)
-    value = 1.0 / per
-    sample = (f"per step: full layout of {R * T} tokens + dispatch and combine of {per_step_tokens} "
-              f"seeded random source tokens of {describe(wl)}; single-threaded C++ oracle")
+            step_s.append(t_layout + t_disp + t_comb)
+            per_token.append(per)
+    value = 1.0 / statistics.mean(per_token)
+    sample = (f"per step: layout of all {R * T} tokens + dispatch and combine of {n_tok} seeded random "
+              f"source tokens of {describe(wl)}; ms_per_step is that sampled work's measured time, value "
+              f"extrapolates it to all {R * T} tokens; single-threaded C++ oracle")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": per * R * T * 1e3, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "fp32 oracle arithmetic", "data": "synthetic",
-            "config": {"workload": describe(wl)},
+            "ms_per_step": statistics.mean(step_s) * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp32 oracle arithmetic", "data": "synthetic (seeded routing and activations)",
+            "config": run_config(wl, args, world, ntpr),
+            "sampled_tokens_per_step": n_tok,
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                             "sample": sample},
+                             "host": host_cpu(), "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 

@@ -26,7 +26,8 @@ EP_DTYPE_BF16, EP_DTYPE_FP8_E4M3 = 0, 1
 
 __all__ = [
     "Config", "Layout", "Recv", "EpError", "lib", "ep_workspace_bytes", "ep_recv_rows",
-    "ep_workspace_init", "ep_get_dispatch_layout", "ep_get_dispatch_layout_noalloc", "ep_dispatch", "ep_combine", "ep_check_error",
+    "ep_workspace_init", "ep_get_dispatch_layout", "ep_get_dispatch_layout_noalloc", "ep_check_error_noalloc",
+    "ep_dispatch", "ep_combine", "ep_check_error",
     "ep_dispatch_atomic", "ep_deterministic_sort",
     "ep_status_string", "ep_diag_e4m3_of_bits", "ep_diag_bf16_of_bits",
     "ep_diag_copy_fanout", "ep_diag_wait_timeout", "use_checked", "alloc_layout", "alloc_recv",
@@ -44,13 +45,14 @@ class _Config(C.Structure):
     _fields_ = [(n, C.c_int32) for n in (
         "num_scaleout_ranks", "num_scaleup_ranks", "num_experts", "num_topk", "num_tokens",
         "num_max_tokens_per_rank", "hidden", "x_dtype", "recv_dtype", "expand", "expert_alignment",
-        "num_sms", "num_prologue_sms", "compact_recv", "zero_padding", "sf_pack", "copy_path")]
+        "num_sms", "num_prologue_sms", "compact_recv", "zero_padding", "sf_pack", "copy_path",
+        "recv_capacity")]
 
 
 class _Layout(C.Structure):
     _fields_ = [(n, C.c_void_p) for n in (
         "num_tokens_per_rank", "num_tokens_per_expert", "is_token_in_rank", "slot_map", "recv_cnt",
-        "recv_psum", "exp_cnt", "exp_base", "exp_region", "exp_pos")]
+        "recv_psum", "exp_cnt", "exp_base", "exp_region", "exp_pos", "recv_region")]
 
 
 class _Recv(C.Structure):
@@ -95,6 +97,7 @@ class Config(_KeepsStruct):
     zero_padding: int = 0
     sf_pack: int = 0
     copy_path: int = 0  # unchanged rows: 0 automatic, 1 register copies, 2 bulk copies
+    recv_capacity: int = 0  # packed receive rows: rows of the receive tensors (0 = R*T*min(K,R))
 
     @property
     def num_ranks(self) -> int:
@@ -111,7 +114,8 @@ def config_of(wl, **over) -> Config:
                EP_DTYPE_FP8_E4M3 if wl.x_dtype == "fp8" else EP_DTYPE_BF16,
                EP_DTYPE_FP8_E4M3 if wl.recv_dtype == "fp8" else EP_DTYPE_BF16,
                int(bool(wl.expand)), wl.expert_alignment,
-               compact_recv=int(bool(getattr(wl, "compact", False))),
+               compact_recv=int(getattr(wl, "compact", 0)),
+               recv_capacity=int(getattr(wl, "recv_capacity", 0)),
                zero_padding=int(bool(getattr(wl, "zero_padding", False))),
                sf_pack=int(bool(getattr(wl, "sf_pack", False))))
     return dataclasses.replace(c, **over)
@@ -149,6 +153,8 @@ def lib():
         L.ep_get_dispatch_layout.argtypes = [P, P, P, P, C.c_size_t, P]
         L.ep_get_dispatch_layout_noalloc.restype = I
         L.ep_get_dispatch_layout_noalloc.argtypes = [P, P, P, P]
+        L.ep_check_error_noalloc.restype = I
+        L.ep_check_error_noalloc.argtypes = [P]
         L.ep_dispatch.restype = I
         L.ep_dispatch.argtypes = [P, P, P, P, P, P, P, P, C.c_size_t, P]
         L.ep_dispatch_atomic.restype = I
@@ -219,6 +225,7 @@ class Layout(_KeepsStruct):
     exp_base: torch.Tensor | None = None
     exp_region: torch.Tensor | None = None
     exp_pos: torch.Tensor | None = None
+    recv_region: torch.Tensor | None = None
 
     def _build_struct(self) -> _Layout:
         return _Layout(*(_ptr(getattr(self, f[0])) for f in _Layout._fields_))
@@ -251,7 +258,7 @@ def alloc_layout(cfg: Config, device="cuda") -> Layout:
     i32 = dict(dtype=torch.int32, device=device)
     lay = Layout(torch.empty(R, R, **i32), torch.empty(R, E, **i32),
                  torch.empty(R, T, R, dtype=torch.uint8, device=device), torch.empty(R, T, K, **i32),
-                 torch.empty(R, R, **i32), torch.empty(R, R, **i32))
+                 torch.empty(R, R, **i32), torch.empty(R, R, **i32), recv_region=torch.empty(R + 1, **i32))
     if cfg.expand:
         lay.exp_cnt = torch.empty(R, L, **i32)
         lay.exp_base = torch.empty(R, L + 1, **i32)
@@ -272,9 +279,11 @@ def alloc_recv(cfg: Config, device="cuda", sidecars: bool = True, zero: bool = F
     recv_sf = mk(rows, (G + 3) // 4 if cfg.sf_pack else G, dtype=torch.float32, device=device) if fp8 else None
     if not sidecars:
         return Recv(recv_x, recv_sf, None, None, None)
-    return Recv(recv_x, recv_sf, mk(R, R * M, K, dtype=torch.int64, device=device),
-                mk(R, R * M, K, dtype=torch.float32, device=device),
-                mk(R, R * M, K + 2, dtype=torch.int32, device=device))
+    # sidecar rows: one region of R*M rows per destination, or the packed rows
+    side = (rows,) if cfg.compact_recv == 2 else (R, R * M)
+    return Recv(recv_x, recv_sf, mk(*side, K, dtype=torch.int64, device=device),
+                mk(*side, K, dtype=torch.float32, device=device),
+                mk(*side, K + 2, dtype=torch.int32, device=device))
 
 
 def ep_get_dispatch_layout(cfg: Config, topk_idx: torch.Tensor, layout: Layout, ws: torch.Tensor,
@@ -289,6 +298,12 @@ def ep_get_dispatch_layout_noalloc(cfg: Config, topk_idx: torch.Tensor, layout: 
     c, l = cfg._c(), layout._c()
     _check(lib().ep_get_dispatch_layout_noalloc(C.byref(c), _ptr(topk_idx), C.byref(l), _stream(stream)),
            "ep_get_dispatch_layout_noalloc")
+
+
+def ep_check_error_noalloc(stream=None) -> int:
+    """Synchronises the stream; returns (and clears) the status the
+    allocation-free layout latched in the library's array."""
+    return int(lib().ep_check_error_noalloc(_stream(stream)))
 
 
 def ep_dispatch(cfg: Config, layout: Layout, x: torch.Tensor, x_sf, topk_idx: torch.Tensor,

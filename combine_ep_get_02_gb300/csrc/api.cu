@@ -114,8 +114,9 @@ int make_geometry(const ep_config_t* c, Geometry* g) {
   if (c->expand != 0 && c->expand != 1) return EP_ERR_INVALID_ARG;
   if (c->expert_alignment < 1) return EP_ERR_INVALID_ARG;
   if (c->num_sms < 0 || c->num_prologue_sms < 0) return EP_ERR_INVALID_ARG;
-  if (c->compact_recv != 0 && c->compact_recv != 1) return EP_ERR_INVALID_ARG;
+  if (c->compact_recv < 0 || c->compact_recv > 2 || c->recv_capacity < 0) return EP_ERR_INVALID_ARG;
   if (c->compact_recv && c->expand) return EP_ERR_UNSUPPORTED;  // expanded rows are packed already
+  if (c->recv_capacity && c->compact_recv != 2) return EP_ERR_UNSUPPORTED;  // only packed rows take one
   if (c->zero_padding != 0 && c->zero_padding != 1) return EP_ERR_INVALID_ARG;
   if (c->zero_padding && !c->expand) return EP_ERR_UNSUPPORTED;  // only expanded blocks are padded
   if (c->sf_pack != 0 && c->sf_pack != 1) return EP_ERR_INVALID_ARG;
@@ -142,12 +143,35 @@ int make_geometry(const ep_config_t* c, Geometry* g) {
   g->expand = c->expand;
   g->align = c->expert_alignment;
   g->compact = c->compact_recv;
+  if (g->compact == 2)  // every token has at most min(K, R) distinct destinations
+    g->entry_rows = c->recv_capacity > 0 ? c->recv_capacity
+                                         : R * c->num_tokens * (c->num_topk < R ? c->num_topk : R);
+  else
+    g->entry_rows = R * region_rows;
   g->zero_padding = c->zero_padding;
   g->sf_pack = c->sf_pack;
   g->copy_path = c->copy_path;
   g->SW = c->sf_pack ? (g->G + 3) / 4 : g->G;
   g->region_rows = region_rows;
   g->num_tokens = R * c->num_tokens;
+  return EP_OK;
+}
+
+int check_layout_args(const Geometry& g, const int64_t* topk_idx, const ep_layout_t* layout) {
+  if (layout == nullptr) return EP_ERR_INVALID_ARG;
+  const bool has_tokens = g.T > 0;
+  if ((has_tokens && (topk_idx == nullptr || layout->is_token_in_rank == nullptr ||
+                      layout->slot_map == nullptr)) ||
+      layout->num_tokens_per_rank == nullptr || layout->num_tokens_per_expert == nullptr ||
+      layout->recv_cnt == nullptr || layout->recv_psum == nullptr)
+    return EP_ERR_INVALID_ARG;
+  if (g.expand && (layout->exp_cnt == nullptr || layout->exp_base == nullptr ||
+                   layout->exp_region == nullptr || (has_tokens && layout->exp_pos == nullptr)))
+    return EP_ERR_INVALID_ARG;
+  if (g.compact == 2 && layout->recv_region == nullptr) return EP_ERR_INVALID_ARG;
+  if (!aligned(topk_idx, 8) || !aligned(layout->slot_map, 4) ||
+      !aligned(layout->is_token_in_rank, 4) || !aligned(layout->num_tokens_per_rank, 4))
+    return EP_ERR_INVALID_ARG;
   return EP_OK;
 }
 
@@ -199,7 +223,7 @@ int64_t ep_recv_rows(const ep_config_t* cfg) {
   if (make_geometry(cfg, &g) != EP_OK) return -1;
   if (g.expand)
     return static_cast<int64_t>(g.R) * g.T * g.K + static_cast<int64_t>(g.E) * (g.align - 1);
-  return static_cast<int64_t>(g.R) * g.region_rows;
+  return g.entry_rows;
 }
 
 int ep_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
@@ -214,19 +238,7 @@ int ep_get_dispatch_layout(const ep_config_t* cfg, const int64_t* topk_idx,
   int st = make_geometry(cfg, &g);
   if (st != EP_OK) return st;
   if ((st = check_workspace(g, workspace, workspace_bytes)) != EP_OK) return st;
-  if (layout == nullptr) return EP_ERR_INVALID_ARG;
-  const bool has_tokens = g.T > 0;
-  if ((has_tokens && (topk_idx == nullptr || layout->is_token_in_rank == nullptr ||
-                      layout->slot_map == nullptr)) ||
-      layout->num_tokens_per_rank == nullptr || layout->num_tokens_per_expert == nullptr ||
-      layout->recv_cnt == nullptr || layout->recv_psum == nullptr)
-    return EP_ERR_INVALID_ARG;
-  if (g.expand && (layout->exp_cnt == nullptr || layout->exp_base == nullptr ||
-                   layout->exp_region == nullptr || (has_tokens && layout->exp_pos == nullptr)))
-    return EP_ERR_INVALID_ARG;
-  if (!aligned(topk_idx, 8) || !aligned(layout->slot_map, 4) ||
-      !aligned(layout->is_token_in_rank, 4) || !aligned(layout->num_tokens_per_rank, 4))
-    return EP_ERR_INVALID_ARG;
+  if ((st = check_layout_args(g, topk_idx, layout)) != EP_OK) return st;
   const Workspace w = workspace_layout(g);
   LayoutArgs a;
   a.topk_idx = topk_idx;
@@ -236,6 +248,7 @@ int ep_get_dispatch_layout(const ep_config_t* cfg, const int64_t* topk_idx,
   a.slot_map = layout->slot_map;
   a.recv_cnt = layout->recv_cnt;
   a.recv_psum = layout->recv_psum;
+  a.recv_region = layout->recv_region;
   a.exp_cnt = layout->exp_cnt;
   a.exp_base = layout->exp_base;
   a.exp_region = layout->exp_region;
@@ -274,6 +287,7 @@ int ep_dispatch(const ep_config_t* cfg, const ep_layout_t* layout, const void* x
   if (g.expand && (layout->exp_pos == nullptr || layout->exp_region == nullptr))
     return EP_ERR_INVALID_ARG;
   if (g.compact && layout->recv_psum == nullptr) return EP_ERR_INVALID_ARG;
+  if (g.compact == 2 && layout->recv_region == nullptr) return EP_ERR_INVALID_ARG;
   if (g.zero_padding && (layout->exp_cnt == nullptr || layout->exp_base == nullptr))
     return EP_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(recv->recv_x, 16) || !aligned(topk_idx, 8) ||
@@ -294,6 +308,7 @@ int ep_dispatch(const ep_config_t* cfg, const ep_layout_t* layout, const void* x
   a.exp_pos = layout->exp_pos;
   a.exp_region = layout->exp_region;
   a.recv_psum = layout->recv_psum;
+  a.recv_region = layout->recv_region;
   a.exp_cnt = layout->exp_cnt;
   a.exp_base = layout->exp_base;
   a.recv_x = static_cast<uint8_t*>(recv->recv_x);
@@ -302,7 +317,8 @@ int ep_dispatch(const ep_config_t* cfg, const ep_layout_t* layout, const void* x
   a.recv_w = recv->recv_topk_weights;
   a.recv_md = recv->recv_src_metadata;
   a.err = at<uint32_t>(workspace, workspace_layout(g).err);
-  a.recv_rows = recv->recv_x_rows;
+  a.recv_rows = g.expand ? recv->recv_x_rows : need_rows;  // packed: the configured capacity
+  a.side_rows = g.entry_rows;
   a.R = g.R;
   a.E = g.E;
   a.L = g.L;
@@ -337,6 +353,7 @@ int ep_combine(const ep_config_t* cfg, const ep_layout_t* layout, const uint16_t
                : layout->slot_map == nullptr)
     return EP_ERR_INVALID_ARG;
   if (g.compact && layout->recv_psum == nullptr) return EP_ERR_INVALID_ARG;
+  if (g.compact == 2 && layout->recv_region == nullptr) return EP_ERR_INVALID_ARG;
   if (!aligned(y, 16) || !aligned(out, 16) || !aligned(topk_idx, 8) || !aligned(topk_weights, 4))
     return EP_ERR_INVALID_ARG;
   const int sms = sms_or_all(cfg->num_sms);
@@ -349,6 +366,7 @@ int ep_combine(const ep_config_t* cfg, const ep_layout_t* layout, const uint16_t
   a.exp_pos = layout->exp_pos;
   a.exp_region = layout->exp_region;
   a.recv_psum = layout->recv_psum;
+  a.recv_region = layout->recv_region;
   a.out = out;
   a.err = at<uint32_t>(workspace, workspace_layout(g).err);
   a.y_rows = ep_recv_rows(cfg);
@@ -397,6 +415,7 @@ int ep_dispatch_atomic(const ep_config_t* cfg, const void* x, const float* x_sf,
   a.recv_w = recv->recv_topk_weights;
   a.recv_md = recv->recv_src_metadata;
   a.recv_rows = recv->recv_x_rows;
+  a.side_rows = g.entry_rows;
   a.R = g.R;
   a.E = g.E;
   a.L = g.L;

@@ -59,11 +59,10 @@ __global__ void __launch_bounds__(kCopyThreads) combine_kernel(CombineArgs a) {
       float w = 0.f;
       if (e >= 0 && e < a.E && r >= 0) {
         const int d = static_cast<int>(e) / a.L;
-        const int64_t row =
-            kExpand ? static_cast<int64_t>(a.exp_region[d]) + r
-                    : static_cast<int64_t>(d) * a.region_rows +
-                          recv_row_of_slot(r, d, a.R, a.M, a.compact, a.recv_psum);
-        if (row_in_bounds(row, a.y_rows, a.err)) {  // checked builds: the lane is dropped
+        const int64_t row = kExpand ? static_cast<int64_t>(a.exp_region[d]) + r : entry_row(a, d, r, a.err);
+        // a packed row past the capacity was never received: the lane is left
+        // out and kErrOverflow latched (checked builds: rows outside y too)
+        if (row_usable(row, a.y_rows, a.compact == 2, a.err)) {
           p = a.y + row * a.H;
           w = w_cur;
         }

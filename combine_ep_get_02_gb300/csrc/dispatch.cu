@@ -30,7 +30,6 @@ __global__ void __launch_bounds__(kCopyThreads) dispatch_kernel(DispatchArgs a) 
   __shared__ int64_t s_row[kWarps][kMaxTopk];               // hidden destination rows
   __shared__ float s_sf[kWarps][kMaxScaleGroups];           // this token's FP8 scales
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const unsigned lt = lanemask_lt();
   const int64_t gwarp = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
 
@@ -42,15 +41,7 @@ __global__ void __launch_bounds__(kCopyThreads) dispatch_kernel(DispatchArgs a) 
     const RawLane cur = next;
     next = fetch_lane(a, tok + nwarps, lane, kExpand, kAtomic);
     const TokenLanes ln = lanes_of(a, cur, tok, lane, kExpand, kAtomic);
-    const unsigned hmask = kExpand ? ln.vmask : ln.rmask;
-    if ((hmask >> lane) & 1) {
-      int64_t row = kExpand ? static_cast<int64_t>(a.exp_region[ln.d]) + ln.pos
-                            : static_cast<int64_t>(ln.d) * a.region_rows + ln.row;
-      if (!row_in_bounds(row, a.recv_rows, a.err)) row = -1;  // checked builds: skipped below
-      s_row[warp][__popc(hmask & lt)] = row;
-    }
-    __syncwarp();
-    const int nh = __popc(hmask);
+    const int nh = hidden_rows(a, ln, lane, kExpand, s_row[warp]);
 
     if (kKind == kCopyRow) {
       // the row's bytes unchanged (bf16 -> bf16, or pre-cast e4m3 -> e4m3)
@@ -64,7 +55,6 @@ __global__ void __launch_bounds__(kCopyThreads) dispatch_kernel(DispatchArgs a) 
           if (c < nchunk) v[u] = ld_stream16(src + (static_cast<size_t>(c) << 4));
         }
         for (int j = 0; j < nh; ++j) {
-          if (kChecked && s_row[warp][j] < 0) continue;
           uint8_t* dst = a.recv_x + s_row[warp][j] * a.out_row_bytes;
 #pragma unroll
           for (int u = 0; u < kUnroll; ++u) {
@@ -77,8 +67,7 @@ __global__ void __launch_bounds__(kCopyThreads) dispatch_kernel(DispatchArgs a) 
         const float* ssrc = a.x_sf + tok * a.SW;
         for (int g = lane; g < a.SW; g += 32) {
           const float v = ssrc[g];
-          for (int j = 0; j < nh; ++j)
-            if (!kChecked || s_row[warp][j] >= 0) a.recv_sf[s_row[warp][j] * a.SW + g] = v;
+          for (int j = 0; j < nh; ++j) a.recv_sf[s_row[warp][j] * a.SW + g] = v;
         }
       }
     } else {
@@ -108,8 +97,7 @@ __global__ void __launch_bounds__(kCopyThreads) dispatch_kernel(DispatchArgs a) 
               else s_sf[warp][u >> 3] = cu.sf;
             }
             for (int j = 0; j < nh; ++j)
-              if (!kChecked || s_row[warp][j] >= 0)
-                st16(a.recv_x + s_row[warp][j] * a.out_row_bytes + (static_cast<size_t>(u) << 4), q);
+              st16(a.recv_x + s_row[warp][j] * a.out_row_bytes + (static_cast<size_t>(u) << 4), q);
           }
         }
       }
@@ -121,15 +109,12 @@ __global__ void __launch_bounds__(kCopyThreads) dispatch_kernel(DispatchArgs a) 
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             if (4 * wd + i < a.G) v |= static_cast<uint32_t>(b[4 * wd + i]) << (8 * i);
-          for (int j = 0; j < nh; ++j)
-            if (!kChecked || s_row[warp][j] >= 0)
-              reinterpret_cast<uint32_t*>(a.recv_sf)[s_row[warp][j] * a.SW + wd] = v;
+          for (int j = 0; j < nh; ++j) reinterpret_cast<uint32_t*>(a.recv_sf)[s_row[warp][j] * a.SW + wd] = v;
         }
       } else {
         for (int g = lane; g < a.G; g += 32) {
           const float v = s_sf[warp][g];
-          for (int j = 0; j < nh; ++j)
-            if (!kChecked || s_row[warp][j] >= 0) a.recv_sf[s_row[warp][j] * a.G + g] = v;
+          for (int j = 0; j < nh; ++j) a.recv_sf[s_row[warp][j] * a.G + g] = v;
         }
       }
     }

@@ -32,7 +32,6 @@ __global__ void __launch_bounds__(kBulkThreads) dispatch_bulk_kernel(DispatchArg
   __shared__ __align__(8) uint64_t bar[kBulkWarps][kBulkStages];
   __shared__ int64_t s_row[kBulkWarps][kMaxTopk];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const unsigned lt = lanemask_lt();
   const int64_t gwarp = static_cast<int64_t>(blockIdx.x) * kBulkWarps + warp;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kBulkWarps;
   const int row_bytes = a.in_row_bytes;  // == out_row_bytes for an unchanged row
@@ -75,15 +74,7 @@ __global__ void __launch_bounds__(kBulkThreads) dispatch_bulk_kernel(DispatchArg
     const RawLane cur = next;
     next = fetch_lane(a, tok + nwarps, lane, kExpand, false);
     const TokenLanes ln = lanes_of(a, cur, tok, lane, kExpand, false);
-    const unsigned hmask = kExpand ? ln.vmask : ln.rmask;
-    if ((hmask >> lane) & 1) {
-      int64_t row = kExpand ? static_cast<int64_t>(a.exp_region[ln.d]) + ln.pos
-                            : static_cast<int64_t>(ln.d) * a.region_rows + ln.row;
-      if (!row_in_bounds(row, a.recv_rows, a.err)) row = -1;  // checked builds: skipped below
-      s_row[warp][__popc(hmask & lt)] = row;
-    }
-    __syncwarp();
-    const int nh = __popc(hmask);
+    const int nh = hidden_rows(a, ln, lane, kExpand, s_row[warp]);
 
     for (int piece = 0; piece < pieces; ++piece) {
       // start the following piece in the other stage
@@ -103,9 +94,7 @@ __global__ void __launch_bounds__(kBulkThreads) dispatch_bulk_kernel(DispatchArg
       if (lane == 0) {
         const int off = piece * stage_bytes;
         const uint32_t n = static_cast<uint32_t>(min(stage_bytes, row_bytes - off));
-        for (int j = 0; j < nh; ++j)
-          if (!kChecked || s_row[warp][j] >= 0)
-            bulk_store(a.recv_x + s_row[warp][j] * a.out_row_bytes + off, st_addr(stage), n);
+        for (int j = 0; j < nh; ++j) bulk_store(a.recv_x + s_row[warp][j] * a.out_row_bytes + off, st_addr(stage), n);
         bulk_commit();
       }
       stage ^= 1;
@@ -116,8 +105,7 @@ __global__ void __launch_bounds__(kBulkThreads) dispatch_bulk_kernel(DispatchArg
       const float* ssrc = a.x_sf + tok * a.SW;
       for (int g = lane; g < a.SW; g += 32) {
         const float v = ssrc[g];
-        for (int j = 0; j < nh; ++j)
-          if (!kChecked || s_row[warp][j] >= 0) a.recv_sf[s_row[warp][j] * a.SW + g] = v;
+        for (int j = 0; j < nh; ++j) a.recv_sf[s_row[warp][j] * a.SW + g] = v;
       }
     }
     write_sidecars(a, ln, s_rank, t, lane, kExpand);

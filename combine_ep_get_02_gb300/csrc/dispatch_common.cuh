@@ -11,7 +11,8 @@ namespace {
 
 struct TokenLanes {
   int e, d, slot, pos;
-  int row;  // receive row of the lane's deduplicated entry inside its destination region
+  int64_t row;  // row of the lane's deduplicated entry in the receive tensors (the
+                // sidecars, and recv_x unless expanded); -1 for an invalid lane
   float w;
   unsigned vmask;  // valid lanes
   unsigned rmask;  // first lane per destination (deduplicated entries)
@@ -67,8 +68,27 @@ __device__ __forceinline__ TokenLanes lanes_of(const DispatchArgs& a, const RawL
     L.slot = __shfl_sync(kFullMask, mine, __ffs(same) - 1);
     if (!valid) L.slot = -1;
   }
-  L.row = (valid && !expand) ? recv_row_of_slot(L.slot, L.d, a.R, a.M, a.compact, a.recv_psum) : -1;
+  L.row = valid ? entry_row(a, L.d, L.slot, a.err) : -1;
   return L;
+}
+
+// The receive rows of recv_x a token's row goes to, gathered into s_row (one
+// per deduplicated entry, or per valid lane when expanded) in lane order;
+// returns how many. A row that may not be written (a packed row past the
+// capacity, or in checked builds one outside the buffer) is left out and its
+// error latched.
+__device__ __forceinline__ int hidden_rows(const DispatchArgs& a, const TokenLanes& ln, int lane, bool expand,
+                                           int64_t* s_row) {
+  const unsigned hmask = expand ? ln.vmask : ln.rmask;
+  int64_t row = -1;
+  if ((hmask >> lane) & 1) {
+    row = expand ? static_cast<int64_t>(a.exp_region[ln.d]) + ln.pos : ln.row;
+    if (!row_usable(row, a.recv_rows, a.compact == 2, a.err)) row = -1;
+  }
+  const unsigned keep = __ballot_sync(kFullMask, row >= 0);
+  if (row >= 0) s_row[__popc(keep & lanemask_lt())] = row;
+  __syncwarp();
+  return __popc(keep);
 }
 
 // One lane's 16 columns of a 128-column group (8 consecutive lanes form a
@@ -133,10 +153,10 @@ __device__ __forceinline__ void write_sidecars(const DispatchArgs& a, const Toke
       const int rl = __ffs(m) - 1;
       m &= m - 1;
       const int dj = __shfl_sync(kFullMask, ln.d, rl);
-      const int row = __shfl_sync(kFullMask, kExpand ? ln.slot : ln.row, rl);
-      const int64_t mrow = static_cast<int64_t>(dj) * a.region_rows + row;
-      if (!row_in_bounds(mrow, static_cast<int64_t>(a.R) * a.region_rows, lane == 0 ? a.err : nullptr))
-        continue;  // checked builds only; the same for every lane
+      const int64_t mrow = __shfl_sync(kFullMask, ln.row, rl);
+      // packed rows past the capacity (and, checked builds, rows outside the
+      // buffer) are skipped; the same for every lane
+      if (!row_usable(mrow, a.side_rows, a.compact == 2, lane == 0 ? a.err : nullptr)) continue;
       if (lane < a.K) {
         const bool on = ln.d == dj;
         if (a.recv_idx) a.recv_idx[mrow * a.K + lane] = on ? static_cast<int64_t>(ln.e - dj * a.L) : -1;

@@ -39,10 +39,13 @@ constexpr bool kChecked = false;
 // Sizes derived from an ep_config_t that passed validation.
 struct Geometry {
   int R, n_so, n_su, E, L, K, T, M, H, G;
-  int x_fp8, recv_fp8, expand, align, compact, zero_padding, sf_pack;
+  int x_fp8, recv_fp8, expand, align, zero_padding, sf_pack;
+  int compact;  // receive rows: 0 at their slots, 1 compact windows, 2 packed back to back
   int copy_path;  // 0 automatic, 1 register copies, 2 bulk copies (rows that travel unchanged)
   int SW;  // 32-bit words of one row's scale sidecar: G, or ceil(G/4) packed
   int64_t region_rows;  // rows of one destination region in the row form: R * M
+  int64_t entry_rows;   // rows of the receive tensors holding deduplicated entries (recv_x
+                        // unless expanded, and the sidecars): R * R * M, or the packed capacity
   int64_t num_tokens;   // R * T
 };
 
@@ -56,6 +59,8 @@ struct Workspace {
 
 Workspace workspace_layout(const Geometry& g);
 int make_geometry(const ep_config_t* cfg, Geometry* g);  // returns EP_OK or an error
+// The layout's pointer arguments (present, aligned): EP_OK or EP_ERR_INVALID_ARG.
+int check_layout_args(const Geometry& g, const int64_t* topk_idx, const ep_layout_t* layout);
 
 struct LayoutArgs {
   const int64_t* topk_idx;
@@ -65,6 +70,7 @@ struct LayoutArgs {
   int32_t* slot_map;
   int32_t* recv_cnt;
   int32_t* recv_psum;
+  int32_t* recv_region;  // may be null
   int32_t* exp_cnt;
   int32_t* exp_base;
   int32_t* exp_region;
@@ -87,7 +93,8 @@ struct DispatchArgs {
   const int32_t* slot_map;
   const int32_t* exp_pos;
   const int32_t* exp_region;
-  const int32_t* recv_psum;  // compact receive rows only
+  const int32_t* recv_psum;    // compact and packed receive rows only
+  const int32_t* recv_region;  // packed receive rows only
   const int32_t* exp_cnt;    // zero padding only
   const int32_t* exp_base;   // zero padding only
   int32_t* send_counters;    // atomic-slot comparison path only: [R src][R dst]
@@ -97,7 +104,8 @@ struct DispatchArgs {
   float* recv_w;
   int32_t* recv_md;
   uint32_t* err;             // the workspace's device error bits (null: none)
-  int64_t recv_rows;         // rows of recv_x and recv_sf (checked builds)
+  int64_t recv_rows;         // rows of recv_x and recv_sf (the capacity when packed)
+  int64_t side_rows;         // rows of the sidecar tensors
   int R, E, L, K, T, H, G, M, compact, zero_padding, n_so, n_su, sf_pack;
   int SW;  // 32-bit words of one row's scale sidecar
   int64_t region_rows;
@@ -131,10 +139,11 @@ struct CombineArgs {
   const int32_t* slot_map;
   const int32_t* exp_pos;
   const int32_t* exp_region;
-  const int32_t* recv_psum;  // compact receive rows only
+  const int32_t* recv_psum;    // compact and packed receive rows only
+  const int32_t* recv_region;  // packed receive rows only
   uint16_t* out;
   uint32_t* err;     // the workspace's device error bits
-  int64_t y_rows;    // rows of y (checked builds)
+  int64_t y_rows;    // rows of y (the capacity when packed)
   int E, L, K, T, H, R, M, compact;
   int splits;        // column ranges per token (work units per token)
   int split_chunks;  // 16-byte chunks per range
@@ -166,15 +175,28 @@ int device_sm_count();
 // runtime call failed.
 int resident_ctas(const void* kernel, int threads, size_t smem);
 
-// Receive row inside destination d's region of a row-form slot: the slot, or
-// (compact) the exclusive prefix of d's receive counts before the slot's row
-// block plus the slot's offset in that block.
-__device__ __forceinline__ int recv_row_of_slot(int slot, int d, int R, int M, int compact,
-                                                const int32_t* recv_psum) {
-  if (!compact) return slot;
-  const int rb = slot / M;
-  const int before = rb == 0 ? 0 : __ldg(recv_psum + d * R + rb - 1);
-  return before + slot - rb * M;
+// Row of a deduplicated (token, destination d) entry with row-form slot
+// `slot` in the receive tensors (Args: DispatchArgs or CombineArgs):
+//   row form  d*R*M + slot;
+//   compact   d*R*M + recv_psum[d][rb-1] + slot - rb*M with rb = slot / M (the
+//             destination's entries packed from the start of its window in
+//             row-block order, PR #690 Direct Recv X; recv_psum[d][-1] = 0);
+//   packed    the same with recv_region[d] (the entries of the destinations
+//             before d) in place of d*R*M.
+// Checked builds test the slot's row block before reading recv_psum: one
+// outside [0, R) latches kErrBounds and gives -1.
+template <class Args>
+__device__ __forceinline__ int64_t entry_row(const Args& a, int d, int slot, uint32_t* err) {
+  const int64_t window = static_cast<int64_t>(d) * a.region_rows;
+  if (a.compact == 0) return window + slot;
+  const int rb = slot / a.M;
+  if (kChecked && (slot < 0 || rb >= a.R)) {
+    if (err != nullptr) atomicOr(err, kErrBounds);
+    return -1;
+  }
+  const int before = rb == 0 ? 0 : __ldg(a.recv_psum + d * a.R + rb - 1);
+  const int64_t base = a.compact == 1 ? window : static_cast<int64_t>(__ldg(a.recv_region + d));
+  return base + before + slot - static_cast<int64_t>(rb) * a.M;
 }
 
 // Checked builds: is row inside [0, rows)? If not, latch kErrBounds (when there
@@ -183,6 +205,19 @@ __device__ __forceinline__ bool row_in_bounds(int64_t row, int64_t rows, uint32_
   if (!kChecked || (row >= 0 && row < rows)) return true;
   if (err != nullptr) atomicOr(err, kErrBounds);
   return false;
+}
+
+// Whether a computed receive row may be accessed. A packed row at or past the
+// capacity (`rows`) is an entry that does not fit: it latches kErrOverflow and
+// is skipped, in every build (never dropped silently). Checked builds also
+// test [0, rows) (kErrBounds); -1 (a row a check already refused) is skipped.
+__device__ __forceinline__ bool row_usable(int64_t row, int64_t rows, bool packed, uint32_t* err) {
+  if (row < 0) return false;
+  if (packed && row >= rows) {
+    if (err != nullptr) atomicOr(err, kErrOverflow);
+    return false;
+  }
+  return row_in_bounds(row, rows, err);
 }
 
 }  // namespace ep

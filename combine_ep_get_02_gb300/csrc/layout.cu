@@ -18,7 +18,8 @@
 //           slot; the expanded layout ranks a lane among its expert's lanes with
 //           per-warp bitmaps of the tokens (source-local position).
 // The last CTA of the grid to finish (a counter in the workspace, no waiting)
-// turns the receive counts into their prefix sums.
+// turns the receive counts into their prefix sums, and the destinations'
+// totals into the first packed row of each destination.
 // Expanded layout only, two more kernels: layout_expert_scan_kernel scans the
 // per-source expert counts down each expert's column (cross-source offsets and
 // per-expert totals); layout_expand_kernel derives the block starts and region
@@ -135,6 +136,7 @@ __global__ void __launch_bounds__(THREADS) layout_kernel(LayoutArgs a) {
   __shared__ uint32_t bal[WARPS][kMaxRanks];
   __shared__ int32_t wbase[WARPS][kMaxRanks];
   __shared__ int32_t s_cnt[kMaxRanks * kMaxRanks];
+  __shared__ int32_t s_tot[kMaxRanks];
   __shared__ bool s_last;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -351,6 +353,28 @@ __global__ void __launch_bounds__(THREADS) layout_kernel(LayoutArgs a) {
       v += carry;
       if (i < R) a.recv_psum[d * R + i] = v;
       carry = __shfl_sync(kFullMask, v, 31);
+    }
+    if (lane == 0) s_tot[d] = carry;
+  }
+  // packed receive rows: destination d starts after everything the
+  // destinations before it receive
+  if (a.recv_region != nullptr) {
+    __syncthreads();
+    if (warp == 0) {
+      int carry = 0;
+      for (int d0 = 0; d0 < R; d0 += 32) {
+        const int d = d0 + lane;
+        const int n = d < R ? s_tot[d] : 0;
+        int v = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int u = __shfl_up_sync(kFullMask, v, o);
+          if (lane >= o) v += u;
+        }
+        if (d < R) a.recv_region[d] = carry + v - n;
+        carry += __shfl_sync(kFullMask, v, 31);
+      }
+      if (lane == 0) a.recv_region[R] = carry;
     }
   }
   if (tid == 0) *a.done = 0u;  // ready for the next call

@@ -49,8 +49,10 @@ extern "C" {
 #define EP_ERR_CUDA (-4)        /* a CUDA launch or runtime call failed      */
 #define EP_ERR_BAD_TOPK (-5)    /* device: top-k value < -1 or >= num_experts,
                                    or a repeated expert in the expanded layout */
-#define EP_ERR_OVERFLOW (-6)    /* a row would not fit (cannot happen when
-                                   num_tokens <= num_max_tokens_per_rank)   */
+#define EP_ERR_OVERFLOW (-6)    /* device: an entry did not fit its receive
+                                   buffer: a packed row past recv_capacity
+                                   (that entry was not written, and combine
+                                   left its lane out)                        */
 #define EP_ERR_TIMEOUT (-7)     /* device: a bounded wait for a bulk copy gave
                                    up (the kernel returned early; its
                                    outputs are incomplete)                   */
@@ -87,10 +89,15 @@ typedef struct ep_config {
                                       capped at 64 [P753 "New API"]. Results never
                                       depend on it.                              */
   int32_t compact_recv;            /* row form only. 0: receive rows at their slots;
-                                      1: each destination's rows packed from row 0 in
-                                      row-block order ([P690] Direct Recv X: the entries
-                                      of row block i start at the exclusive prefix
-                                      recv_psum[d][i-1] of the receive counts)    */
+                                      1 (compact): each destination's rows packed from
+                                      the start of its R*M-row window in row-block
+                                      order ([P690] Direct Recv X: the entries of row
+                                      block i start at the exclusive prefix
+                                      recv_psum[d][i-1] of the receive counts);
+                                      2 (packed): the same order with the destinations
+                                      back to back in one buffer of recv_capacity rows
+                                      (destination d from layout.recv_region[d]), so
+                                      the receive tensors hold only what can arrive */
   int32_t zero_padding;            /* expanded only: 1 = dispatch writes zeros into the
                                       rows between each expert's lanes and the next
                                       expert_alignment boundary (and their FP8
@@ -111,6 +118,12 @@ typedef struct ep_config {
                                       1 = 16-byte register loads and stores; 2 = bulk
                                       copies through shared memory. Results never
                                       depend on it; the fused cast ignores it.     */
+  int32_t recv_capacity;           /* packed rows only (compact_recv = 2): rows of the
+                                      receive tensors; 0 = R*T*min(K, R), the most
+                                      that can arrive (every token has at most min(K,R)
+                                      destinations). An entry past it is not written
+                                      and latches EP_ERR_OVERFLOW; layout.recv_region[R]
+                                      gives the exact count after the layout.      */
 } ep_config_t;
 
 /* ---- dispatch layout (all device pointers, int32 unless noted) -------------
@@ -142,48 +155,61 @@ typedef struct ep_layout {
   int32_t* exp_region; /* [R+1]: first row of each region; [R] = total rows     */
   int32_t* exp_pos;    /* [R][T][K]: row of the lane inside its destination's
                           region, -1 for masked lanes                          */
+  int32_t* recv_region; /* [R+1] (may be NULL unless compact_recv = 2): first
+                           packed row of each destination = the entries all
+                           destinations before it receive; [R] = total entries */
 } ep_layout_t;
 
 /* ---- receive buffers (device pointers) -------------------------------------
  * Row form: recv_x/recv_sf and the sidecars' rows are indexed d*R*M + slot;
  * compact (compact_recv = 1): d*R*M + recv_psum[d][rb-1] + slot - rb*M with
  * rb = slot / M (recv_psum[d][-1] = 0), so destination d's rows are
- * [d*R*M, d*R*M + sum_s recv_cnt[d][s]). Expanded: recv_x and recv_sf rows are
- * indexed exp_region[d] + exp_pos; the sidecars stay in the row form. Rows no entry fills are left untouched. recv_topk_idx,
- * recv_topk_weights and recv_src_metadata may be NULL (not written).
+ * [d*R*M, d*R*M + sum_s recv_cnt[d][s]); packed (compact_recv = 2):
+ * recv_region[d] + recv_psum[d][rb-1] + slot - rb*M, so destination d's rows
+ * are [recv_region[d], recv_region[d+1]) and all tensors have ep_recv_rows()
+ * rows. Expanded: recv_x and recv_sf rows are indexed exp_region[d] + exp_pos;
+ * the sidecars stay in the row form. Rows no entry fills are left untouched.
+ * recv_topk_idx, recv_topk_weights and recv_src_metadata may be NULL (not
+ * written).
  */
 typedef struct ep_recv {
   void* recv_x;                /* [recv_x_rows][H] bf16 or e4m3                 */
   float* recv_sf;              /* [recv_x_rows][H/128] fp32, or [recv_x_rows][ceil(H/512)]
                                   packed words with sf_pack (FP8 receive only)   */
-  int64_t* recv_topk_idx;      /* [R][R*M][K]: destination-local expert or -1    */
-  float* recv_topk_weights;    /* [R][R*M][K]: weight, or 0 off this destination */
-  int32_t* recv_src_metadata;  /* [R][R*M][2+K]: {src rank, src token,
+  int64_t* recv_topk_idx;      /* [R][R*M][K] (packed: [ep_recv_rows][K]):
+                                  destination-local expert or -1                 */
+  float* recv_topk_weights;    /* same rows x K: weight, or 0 off this destination */
+  int32_t* recv_src_metadata;  /* same rows x (2+K): {src rank, src token,
                                   dst_tensor_idx[K]}; field 2+k = expanded row of
                                   lane k in this destination's region, else -1
                                   [P690 copy-epilogue review]                   */
   int64_t recv_x_rows;         /* capacity of recv_x in rows, >= ep_recv_rows()  */
 } ep_recv_t;
 
-/* Workspace bytes the three entry points need for this configuration. The
- * workspace must be zero-filled before its first use (ep_workspace_init or a
- * zeroing allocator); afterwards the library keeps it consistent. One
- * workspace serves one stream at a time. */
+/* Workspace bytes the three entry points need for this configuration (the
+ * library's own convention: the pages' buffers are transport windows with no
+ * single-GPU counterpart). The workspace must be zero-filled before its first
+ * use (ep_workspace_init or a zeroing allocator); afterwards the library keeps
+ * it consistent. One workspace serves one stream at a time. */
 size_t ep_workspace_bytes(const ep_config_t* cfg);
 
-/* Rows the receive buffer recv_x needs: R*R*M (row form; the per-destination
- * window of [P690]'s buffer sizing times R), or R*T*K + E*(expert_alignment-1)
- * (expanded upper bound). Returns -1 for an invalid configuration. */
+/* Rows the receive buffer recv_x needs: R*R*M (row form and compact; the
+ * per-destination window of [P690]'s buffer sizing times R), recv_capacity or
+ * R*T*min(K, R) (packed), or R*T*K + E*(expert_alignment-1) (expanded upper
+ * bound). Returns -1 for an invalid configuration. */
 int64_t ep_recv_rows(const ep_config_t* cfg);
 
-/* Zero the workspace on `stream`. */
+/* Zero the workspace on `stream` (the library's own convention). */
 int ep_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
 
 /* Dispatch layout [P753 Motivation, Approach]: turns topk_idx (device, int64
  * [R][T][K]; -1 = masked lane) into the counts, the per-lane slots and, when
- * expanding, the per-expert positions of `layout` (all device outputs). Three
- * kernels: a per-block count, a grid-wide scan, then per-lane slots; the
- * result is a pure function of topk_idx. */
+ * expanding, the per-expert positions of `layout` (all device outputs). One
+ * kernel with a thread-block cluster per source rank: per-warp counts, a scan
+ * of the CTAs' counts through distributed shared memory, then per-lane slots;
+ * its last CTA writes the receive prefix sums (and recv_region). The expanded
+ * layout adds two small kernels (the per-expert scan across sources, then the
+ * final positions). The result is a pure function of topk_idx. */
 int ep_get_dispatch_layout(const ep_config_t* cfg, const int64_t* topk_idx,
                            const ep_layout_t* layout, void* workspace,
                            size_t workspace_bytes, void* stream);
@@ -200,15 +226,25 @@ int ep_get_dispatch_layout(const ep_config_t* cfg, const int64_t* topk_idx,
  *   - Outputs, layout and errors for invalid arguments are those of
  *     ep_get_dispatch_layout; a configuration whose ep_workspace_bytes exceeds
  *     EP_NOALLOC_SCRATCH_BYTES returns EP_ERR_WORKSPACE.
- *   - Allocates nothing. The first call on a device (that device current)
- *     looks up the array's device address; make it before any stream capture.
- *   - All calls share the array: each call clears its error bits and counter
- *     on `stream` first; calls that overlap on the GPU race on it.
+ *   - Allocates nothing. The first call in a CUDA context (that context
+ *     current) looks up the array's device address; make it before any stream
+ *     capture. A device reset gives a new context, and the next call looks the
+ *     address up again.
+ *   - All calls share the array: each call, once its arguments have passed
+ *     the checks, clears the array's error bits and counter on `stream`
+ *     first; calls that overlap on the GPU race on it.
  *   - Invalid top-k values are treated as masked lanes, as in
- *     ep_get_dispatch_layout, but they are not reported: there is no
- *     workspace for ep_check_error to read. */
+ *     ep_get_dispatch_layout, and latched in the array's error word, which
+ *     ep_check_error_noalloc reads. */
 int ep_get_dispatch_layout_noalloc(const ep_config_t* cfg, const int64_t* topk_idx,
                                    const ep_layout_t* layout, void* stream);
+
+/* ep_check_error for ep_get_dispatch_layout_noalloc (no counterpart on the
+ * pages): synchronises `stream`, returns the first device-detected error the
+ * allocation-free layout latched in the library's array since the last call
+ * (EP_OK if none) and clears it. Allocates nothing; shares the array, and its
+ * race with overlapping calls, with ep_get_dispatch_layout_noalloc. */
+int ep_check_error_noalloc(void* stream);
 
 /* Dispatch: for every deduplicated (token, destination) entry writes the
  * token's hidden row into the destination's receive rows at its slot (row
@@ -260,10 +296,12 @@ int ep_deterministic_sort(const ep_config_t* cfg, const ep_recv_t* recv,
                           const int32_t* send_counters, const ep_recv_t* sorted, void* stream);
 
 /* Synchronises `stream`, returns the first device-detected error latched in
- * the workspace since the last call (EP_OK if none) and clears it. */
+ * the workspace since the last call (EP_OK if none) and clears it. The
+ * library's own convention (the pages print and continue on a device error;
+ * PR #690's review asks that nothing be dropped silently). */
 int ep_check_error(void* workspace, void* stream);
 
-/* Human-readable name of a status code (static storage). */
+/* Human-readable name of a status code (static storage; the library's own). */
 const char* ep_status_string(int status);
 
 /* Diagnostics: the device's fp32 -> e4m3 (round to nearest even, saturating)

@@ -10,7 +10,7 @@ import oracle
 import workloads as W
 
 LAYOUT_KEYS = ("num_tokens_per_rank", "num_tokens_per_expert", "is_token_in_rank", "slot_map",
-               "recv_cnt", "recv_psum")
+               "recv_cnt", "recv_psum", "recv_region")
 EXPAND_KEYS = ("exp_cnt", "exp_base", "exp_region", "exp_pos")
 
 

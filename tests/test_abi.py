@@ -65,6 +65,11 @@ def test_recv_rows_closed_forms(ep):
     # expanded: every lane plus the worst-case padding of every expert block
     assert ep.ep_recv_rows(cfg(ep, expand=1)) == 16 * 4096 * 8
     assert ep.ep_recv_rows(cfg(ep, expand=1, expert_alignment=128)) == 16 * 4096 * 8 + 256 * 127
+    # compact: the same windows; packed: the most rows that can arrive, R*T*min(K, R)
+    assert ep.ep_recv_rows(cfg(ep, compact_recv=1)) == 16 * 16 * 4096
+    assert ep.ep_recv_rows(cfg(ep, compact_recv=2)) == 16 * 4096 * 8
+    assert ep.ep_recv_rows(cfg(ep, compact_recv=2, num_topk=20)) == 16 * 4096 * 16
+    assert ep.ep_recv_rows(cfg(ep, compact_recv=2, recv_capacity=1234)) == 1234
 
 
 def test_workspace_bytes_closed_form(ep):
@@ -92,8 +97,11 @@ def test_workspace_bytes_closed_form(ep):
     (dict(num_experts=8192), -2),
     (dict(expert_alignment=0), -1),
     (dict(x_dtype=7), -1),
-    (dict(compact_recv=2), -1),
+    (dict(compact_recv=3), -1),
     (dict(compact_recv=1, expand=1), -2),     # expanded rows are packed already
+    (dict(compact_recv=2, expand=1), -2),
+    (dict(recv_capacity=-1, compact_recv=2), -1),
+    (dict(recv_capacity=100), -2),            # a capacity only for packed rows
     (dict(zero_padding=1), -2),               # only expanded blocks have padding
     (dict(zero_padding=3, expand=1), -1),
     (dict(sf_pack=1), -2),                    # packed scales need an FP8 receive
@@ -109,6 +117,23 @@ def test_invalid_configs_are_rejected_before_any_launch(ep, bad, code):
     lay = ep._Layout()
     st = ep.lib().ep_get_dispatch_layout(C.byref(cc), None, C.byref(lay), None, 0, None)
     assert st == code
+
+
+def test_noalloc_checks_arguments_before_touching_the_device(ep):
+    """The allocation-free layout refuses bad arguments before any CUDA call
+    (without a GPU a call that got that far would answer EP_ERR_CUDA), so a
+    refused call never writes the library's shared array."""
+    L = ep.lib()
+    c = cfg(ep)
+    cc = c._c()
+    lay = ep._Layout()
+    assert L.ep_get_dispatch_layout_noalloc(C.byref(cc), C.c_void_p(0x20000), None, None) == ep.EP_ERR_INVALID_ARG
+    assert L.ep_get_dispatch_layout_noalloc(C.byref(cc), C.c_void_p(0x20000), C.byref(lay), None) == \
+        ep.EP_ERR_INVALID_ARG
+    bad = cfg(ep, num_experts=250)._c()
+    assert L.ep_get_dispatch_layout_noalloc(C.byref(bad), None, C.byref(lay), None) == ep.EP_ERR_INVALID_ARG
+    big = cfg(ep, num_scaleup_ranks=64, num_experts=4096, expand=1, num_tokens=16, num_max_tokens_per_rank=16)._c()
+    assert L.ep_get_dispatch_layout_noalloc(C.byref(big), None, C.byref(lay), None) == ep.EP_ERR_WORKSPACE
 
 
 def test_workspace_checks(ep):

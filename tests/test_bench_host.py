@@ -10,6 +10,8 @@ import json
 import os
 import subprocess
 import sys
+import time
+from types import SimpleNamespace
 
 import numpy as np
 import pytest
@@ -73,9 +75,11 @@ def test_algorithmic_bytes_equal_what_the_oracle_moves(name):
 
 
 def test_reference_arm_prints_one_contract_line():
+    t0 = time.perf_counter()
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
                         "tiny_direct", "--steps", "2", "--warmup", "1"], capture_output=True, text=True,
                        timeout=600, cwd=ROOT)
+    wall_s = time.perf_counter() - t0
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
     assert len(lines) == 1
@@ -86,3 +90,11 @@ def test_reference_arm_prints_one_contract_line():
     assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+    # the native arm's config, key for key (the tiny workload's layout gives the dedup rows)
+    wl = W.WORKLOADS["tiny_direct"]
+    idx, _ = W.routing(wl)
+    st, lay = oracle.layout(wl, idx)
+    args = SimpleNamespace(cached=False, copy_path=0)
+    assert d["config"] == bench.run_config(wl, args, 1, int(lay["num_tokens_per_rank"].sum()))
+    # ms_per_step is time actually measured: the timed steps fit in the run's own wall clock
+    assert d["ms_per_step"] * d["steps"] < wall_s * 1e3

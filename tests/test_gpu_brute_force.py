@@ -36,7 +36,10 @@ SHAPES = {
     # 2 scale-out x 2 scale-up row form
     "hybrid_2x2": W.Workload("bf_hybrid_2x2", 2, 2, E, K, T, 4, 8),
     # compact receive rows
-    "compact_r2": W.Workload("bf_compact_r2", 1, 2, E, K, T, 5, 8, compact=True),
+    "compact_r2": W.Workload("bf_compact_r2", 1, 2, E, K, T, 5, 8, compact=1),
+    # packed receive rows (destinations back to back), direct and hybrid
+    "packed_r2": W.Workload("bf_packed_r2", 1, 2, E, K, T, 5, 8, compact=2),
+    "packed_hybrid_2x2": W.Workload("bf_packed_hybrid_2x2", 2, 2, E, K, T, 4, 8, compact=2),
     # fused bf16 -> FP8 cast with fp32 scales, hybrid
     "fp8_hybrid": W.Workload("bf_fp8_hybrid", 2, 2, E, K, T, T, 128, recv_dtype="fp8"),
     # expanded per-expert blocks, alignment 2, zeroed padding
@@ -104,7 +107,7 @@ def test_every_routing_matches_the_oracle(name, copy_path):
         assert st == 0
         got = {k: getattr(lay, k).cpu().numpy() for k in
                ("num_tokens_per_rank", "num_tokens_per_expert", "is_token_in_rank", "slot_map",
-                "recv_cnt", "recv_psum")}
+                "recv_cnt", "recv_psum", "recv_region")}
         if wl.expand:
             got.update({k: getattr(lay, k).cpu().numpy() for k in
                         ("exp_cnt", "exp_base", "exp_region", "exp_pos")})

@@ -10,7 +10,9 @@ no index leaves its buffer:
   report no bounds error and must still match the oracle bit for bit;
 - a layout corrupted on the host (a token's slots or expanded rows pushed far
   past the receive buffer) must come back as EP_ERR_BOUNDS from dispatch and
-  from combine, with every other token still exact. Only the checked build is
+  from combine, with every other token still exact. In the compact and packed
+  layouts such a slot names a row block past the last, and the check comes
+  before the receive prefix sums are read with it. Only the checked build is
   given such input: its checks sit in front of every access that uses them.
 """
 import numpy as np
@@ -60,7 +62,9 @@ def test_parity_case_has_no_bounds_error(name, copy_path):
 
 
 @pytest.mark.parametrize("name,copy_path", [("direct_zipf", 1), ("direct_zipf", 2), ("dsv3_fp8", 0),
-                                            ("expanded", 1), ("expanded", 2)])
+                                            ("expanded", 1), ("expanded", 2),
+                                            ("direct_zipf_compact", 1), ("hybrid_compact", 2),
+                                            ("hybrid_packed", 1), ("dsv3_fp8_packed_rows", 0)])
 def test_corrupted_layout_is_reported_not_written(name, copy_path):
     wl = W.PARITY[name]
     R, T, K = wl.num_ranks, wl.num_tokens, wl.num_topk

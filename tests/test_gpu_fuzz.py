@@ -2,7 +2,7 @@
 
 Each case draws a small configuration (ranks, scale-out split, experts per rank,
 top-k, tokens, max tokens, hidden, input/receive dtypes, expanded or row form,
-alignment and zero padding, compact rows, packed scales, masking, the way unchanged
+alignment and zero padding, compact and packed rows, packed scales, masking, the way unchanged
 rows are copied) from a seeded generator, runs layout -> dispatch -> combine through the C ABI and compares
 every output with the oracle: layouts, every row of the receive buffers (which
 start filled with 0xFF, so untouched rows must stay 0xFF and padding rows must
@@ -45,7 +45,7 @@ def draw(seed):
     return W.Workload(
         f"fuzz{seed}", n_so, n_su, E, K, T, M, H, x_dtype=x_dtype, recv_dtype=recv, expand=expand,
         expert_alignment=align, zero_padding=expand and bool(rng.random() < 0.5),
-        compact=(not expand) and bool(rng.random() < 0.4),
+        compact=0 if expand else int(rng.choice([0, 0, 0, 1, 2])),
         sf_pack=recv == "fp8" and bool(rng.random() < 0.4),
         routing=str(rng.choice(["gauss", "zipf"])), mask_frac=float(rng.choice([0.0, 0.1, 0.5])),
         y_kind="random", seed=seed)

@@ -323,7 +323,7 @@ def test_atomic_slots_plus_sort_equal_the_deterministic_dispatch(name):
         assert torch.equal(a.view(torch.uint8), b.view(torch.uint8)), f
 
 
-@pytest.mark.parametrize("name", ["dsv3_fp8", "expanded", "hybrid_compact"])
+@pytest.mark.parametrize("name", ["dsv3_fp8", "expanded", "hybrid_compact", "hybrid_packed"])
 def test_cuda_graph_replay_equals_eager(name):
     """layout -> dispatch -> combine captured once in a CUDA graph and replayed
     gives the eager results bit for bit (the workspace counter returns to zero
@@ -356,3 +356,44 @@ def test_cuda_graph_replay_equals_eager(name):
     assert_layout_equal(run.layout_np(), eager.layout_np(), wl.expand)
     assert torch.equal(run.recv.recv_x.view(torch.uint8), eager.recv.recv_x.view(torch.uint8))
     assert torch.equal(run.out.view(torch.int16), eager.out.view(torch.int16))
+
+
+@pytest.mark.parametrize("name", ["hybrid_packed", "dsv3_fp8_packed_rows"])
+def test_packed_capacity_overflow_is_reported(name):
+    """Packed receive rows in a buffer smaller than what arrives: the entries
+    past the capacity are not written and dispatch reports EP_ERR_OVERFLOW
+    (PR #690 review: a payload is never dropped silently); every row below the
+    capacity is the oracle's, and combine, which cannot read the lost lanes,
+    reports the same and sums the rest exactly as the oracle does."""
+    base = W.PARITY[name]
+    idx, w, x, sf = inputs(base)
+    st, olay = oracle.layout(base, idx)
+    total = int(olay["recv_region"][-1])
+    wl = base.replace(recv_capacity=total - 37)
+    cap = total - 37
+    run = GpuRun(wl, idx, w, x, sf).layout()
+    assert run.status() == ep.EP_OK
+    assert int(run.lay.recv_region[-1]) == total
+    run.recv = ep.alloc_recv(run.cfg, run.dev)
+    assert run.recv.recv_x.shape[0] == cap
+    for t in (run.recv.recv_x, run.recv.recv_sf, run.recv.recv_topk_idx, run.recv.recv_topk_weights,
+              run.recv.recv_src_metadata):
+        if t is not None:
+            t.view(torch.uint8).fill_(0xFF)
+    run.dispatch()
+    assert run.status() == ep.EP_ERR_OVERFLOW
+    assert run.status() == ep.EP_OK
+    st, orec = oracle.dispatch(wl, olay, x, sf, idx, w, fill=0xFF)
+    assert st == oracle.OVERFLOW
+    row_bytes = wl.hidden * (1 if wl.recv_dtype == "fp8" else 2)
+    got = run.recv.recv_x.contiguous().view(torch.uint8).cpu().numpy().reshape(cap, row_bytes)
+    assert np.array_equal(got, np.ascontiguousarray(orec["recv_x"]).view(np.uint8).reshape(cap, row_bytes))
+    for k in ("recv_topk_idx", "recv_topk_weights", "recv_src_metadata"):
+        g = getattr(run.recv, k).cpu().numpy()
+        assert np.array_equal(g.view(np.uint8), orec[k].view(np.uint8)), k
+    y = random_y(wl, cap, run.dev)
+    run.combine(y)
+    assert run.status() == ep.EP_ERR_OVERFLOW
+    st, o_out = oracle.combine(wl, olay, u16(y), idx, w)
+    assert st == oracle.OVERFLOW
+    assert np.array_equal(u16(run.out), o_out)

@@ -1,7 +1,9 @@
 """The allocation-free layout entry point, for callers that may not allocate
 device memory (for example engine plugins handed only their buffers): it must
 give exactly the layout of ep_get_dispatch_layout, call after call, while its
-scratch lives in a fixed array inside the library instead of a workspace.
+scratch lives in a fixed array inside the library instead of a workspace; the
+device's free memory must not move across its calls; and the device-detected
+errors it latches in that array must reach ep_check_error_noalloc.
 
 Kept in a file of its own that pytest collects last."""
 import pytest
@@ -44,6 +46,43 @@ def test_noalloc_layout_matches_the_workspace_entry_point(name):
     ep.ep_dispatch(ref.cfg, lay, ref.x, ref.sf, ref.idx, ref.w, other, ref.ws)
     torch.cuda.synchronize()
     assert torch.equal(ref.recv.recv_x.view(torch.int16), other.recv_x.view(torch.int16))
+
+
+def test_noalloc_allocates_nothing():
+    """Free device memory (cudaMemGetInfo) is the same before and after a run of
+    calls: the scratch is the library's static array, nothing is allocated."""
+    wl = W.PARITY["expanded"]
+    idx, w, x, sf = inputs(wl)
+    cfg = ep.config_of(wl)
+    lay = ep.alloc_layout(cfg, "cuda")
+    idx_d = idx.to("cuda")
+    ep.ep_get_dispatch_layout_noalloc(cfg, idx_d, lay)  # first call: the module is loaded
+    torch.cuda.synchronize()
+    free_before, _ = torch.cuda.mem_get_info()
+    for _ in range(5):
+        ep.ep_get_dispatch_layout_noalloc(cfg, idx_d, lay)
+    torch.cuda.synchronize()
+    free_after, _ = torch.cuda.mem_get_info()
+    assert free_after == free_before
+    assert ep.ep_check_error_noalloc() == ep.EP_OK
+
+
+def test_noalloc_reports_bad_topk_values():
+    """A top-k value outside [-1, E) is masked, as in the workspace entry point,
+    and reported once through ep_check_error_noalloc."""
+    wl = W.Workload("bad_noalloc", 1, 4, 16, 2, 30, 30, 128)
+    idx, w, x, sf = inputs(wl)
+    idx = idx.clone()
+    idx[1, 3, 0] = 16
+    ref = GpuRun(wl, idx, w, x, sf).layout()
+    assert ref.status() == ep.EP_ERR_BAD_TOPK
+    lay = ep.alloc_layout(ref.cfg, ref.dev)
+    _poison(lay)
+    ep.ep_get_dispatch_layout_noalloc(ref.cfg, ref.idx, lay)
+    assert ep.ep_check_error_noalloc() == ep.EP_ERR_BAD_TOPK
+    assert ep.ep_check_error_noalloc() == ep.EP_OK  # read once, then cleared
+    got = {k: getattr(lay, k).cpu().numpy() for k in ref.layout_np()}
+    assert_layout_equal(got, ref.layout_np(), False)
 
 
 def test_noalloc_rejects_configs_beyond_its_scratch():
