@@ -158,7 +158,7 @@ def lib():
         L.ep_dispatch.restype = I
         L.ep_dispatch.argtypes = [P, P, P, P, P, P, P, P, C.c_size_t, P]
         L.ep_dispatch_atomic.restype = I
-        L.ep_dispatch_atomic.argtypes = [P, P, P, P, P, P, P, P]
+        L.ep_dispatch_atomic.argtypes = [P, P, P, P, P, P, P, P, C.c_size_t, P]
         L.ep_deterministic_sort.restype = I
         L.ep_deterministic_sort.argtypes = [P, P, P, P, P]
         L.ep_combine.restype = I
@@ -315,11 +315,13 @@ def ep_dispatch(cfg: Config, layout: Layout, x: torch.Tensor, x_sf, topk_idx: to
 
 
 def ep_dispatch_atomic(cfg: Config, x: torch.Tensor, x_sf, topk_idx: torch.Tensor,
-                       topk_weights: torch.Tensor, recv: Recv, send_counters: torch.Tensor, stream=None):
+                       topk_weights: torch.Tensor, recv: Recv, send_counters: torch.Tensor, ws: torch.Tensor,
+                       stream=None):
     """Comparison path: dispatch with racing atomicAdd slots (no layout)."""
     c, r = cfg._c(), recv._c()
     _check(lib().ep_dispatch_atomic(C.byref(c), _ptr(x), _ptr(x_sf), _ptr(topk_idx), _ptr(topk_weights),
-                                    C.byref(r), _ptr(send_counters), _stream(stream)), "ep_dispatch_atomic")
+                                    C.byref(r), _ptr(send_counters), _ptr(ws), ws.numel(), _stream(stream)),
+           "ep_dispatch_atomic")
 
 
 def ep_deterministic_sort(cfg: Config, recv: Recv, send_counters: torch.Tensor, sorted_recv: Recv,

@@ -179,6 +179,8 @@ Workspace workspace_layout(const Geometry& g) {
   Workspace w;
   w.err = 0;
   w.done = 4;
+  w.dispatch_queue = 8;
+  w.combine_queue = 24;
   w.exp_off = 256;
   const size_t off_bytes = g.expand ? sizeof(int32_t) * static_cast<size_t>(g.R) * g.E : 0;
   w.total = 256 + ((off_bytes + 255) & ~static_cast<size_t>(255));
@@ -200,6 +202,10 @@ int check_workspace(const Geometry& g, void* ws, size_t ws_bytes) {
 template <typename T>
 T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+WorkQueue work_queue(void* ws, size_t off) {
+  return WorkQueue{at<unsigned long long>(ws, off), at<unsigned long long>(ws, off + 8)};
 }
 
 int sms_or_all(int requested) {
@@ -317,6 +323,7 @@ int ep_dispatch(const ep_config_t* cfg, const ep_layout_t* layout, const void* x
   a.recv_w = recv->recv_topk_weights;
   a.recv_md = recv->recv_src_metadata;
   a.err = at<uint32_t>(workspace, workspace_layout(g).err);
+  a.queue = work_queue(workspace, workspace_layout(g).dispatch_queue);
   a.recv_rows = g.expand ? recv->recv_x_rows : need_rows;  // packed: the configured capacity
   a.side_rows = g.entry_rows;
   a.R = g.R;
@@ -369,6 +376,7 @@ int ep_combine(const ep_config_t* cfg, const ep_layout_t* layout, const uint16_t
   a.recv_region = layout->recv_region;
   a.out = out;
   a.err = at<uint32_t>(workspace, workspace_layout(g).err);
+  a.queue = work_queue(workspace, workspace_layout(g).combine_queue);
   a.y_rows = ep_recv_rows(cfg);
   a.E = g.E;
   a.L = g.L;
@@ -385,11 +393,12 @@ int ep_combine(const ep_config_t* cfg, const ep_layout_t* layout, const uint16_t
 
 int ep_dispatch_atomic(const ep_config_t* cfg, const void* x, const float* x_sf,
                        const int64_t* topk_idx, const float* topk_weights, const ep_recv_t* recv,
-                       int32_t* send_counters, void* stream) {
+                       int32_t* send_counters, void* workspace, size_t workspace_bytes, void* stream) {
   Geometry g;
   int st = make_geometry(cfg, &g);
   if (st != EP_OK) return st;
   if (g.expand || g.compact || g.zero_padding) return EP_ERR_UNSUPPORTED;
+  if ((st = check_workspace(g, workspace, workspace_bytes)) != EP_OK) return st;
   if (recv == nullptr || send_counters == nullptr) return EP_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(send_counters, 0, sizeof(int32_t) * g.R * g.R, s) != cudaSuccess) return EP_ERR_CUDA;
@@ -409,6 +418,8 @@ int ep_dispatch_atomic(const ep_config_t* cfg, const void* x, const float* x_sf,
   a.topk_idx = topk_idx;
   a.topk_w = topk_weights;
   a.send_counters = send_counters;
+  a.err = at<uint32_t>(workspace, workspace_layout(g).err);
+  a.queue = work_queue(workspace, workspace_layout(g).dispatch_queue);
   a.recv_x = static_cast<uint8_t*>(recv->recv_x);
   a.recv_sf = recv->recv_sf;
   a.recv_idx = recv->recv_topk_idx;

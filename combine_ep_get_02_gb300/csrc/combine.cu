@@ -21,15 +21,16 @@ __global__ void __launch_bounds__(kCopyThreads) combine_kernel(CombineArgs a) {
   __shared__ const uint16_t* s_ptr[kWarps][kMaxK];
   __shared__ float s_w[kWarps][kMaxK];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t gwarp = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
   const int nchunk = a.H >> 3;  // 8 bf16 per chunk
 
   // A work unit is one token's column range (a token is split into a.splits
   // ranges of a.split_chunks 16-byte chunks when tokens are too few to keep
-  // every warp busy to the end). Lane k of the warp carries top-k lane k of
-  // the unit's token; the next unit's routing (expert, slot or position,
-  // weight) is loaded while the current unit's rows stream.
+  // every warp busy to the end). Warps take units from the workspace's work
+  // queue (a token's cost grows with its number of valid lanes). Lane k of the
+  // warp carries top-k lane k of the unit's token; the next unit is taken, and
+  // its routing (expert, slot or position, weight) loaded, while the current
+  // unit's rows stream.
   const int64_t units = a.num_tokens * a.splits;
   int64_t e_next = -1;
   int r_next = -1;
@@ -45,15 +46,19 @@ __global__ void __launch_bounds__(kCopyThreads) combine_kernel(CombineArgs a) {
       w_next = __ldg(a.topk_w + i);
     }
   };
-  load_raw(gwarp);
-  for (int64_t unit = gwarp; unit < units; unit += nwarps) {
+  const int64_t gwarp = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
+  UnitStream us = start_units(gwarp, nwarps, units);
+  load_raw(us.cur);
+  while (us.cur < units) {
+    const int64_t unit = us.cur;
     const int64_t tok = unit / a.splits;
     const int c_begin = static_cast<int>(unit - tok * a.splits) * a.split_chunks;
     const int c_end = min(nchunk, c_begin + a.split_chunks);
     const int64_t e = e_next;
     const int r = r_next;
     const float w_cur = w_next;
-    load_raw(unit + nwarps);
+    const int64_t after = take_unit(us, a.queue, lane);
+    load_raw(us.nxt);
     if (lane < kMaxK) {
       const uint16_t* p = nullptr;
       float w = 0.f;
@@ -115,7 +120,9 @@ __global__ void __launch_bounds__(kCopyThreads) combine_kernel(CombineArgs a) {
       }
     }
     __syncwarp();  // s_ptr / s_w are rewritten by the next unit
+    advance_units(us, after);
   }
+  leave_queue(us, a.queue, lane);
 }
 
 template <bool kExpand, int kMaxK, int kSteps>

@@ -5,7 +5,10 @@
 // loads, each lane a strided set of chunks), optionally casts it to FP8-e4m3
 // in registers, and stores it to each destination row; the slots come from the
 // layout (PR #753, Approach: the kernel replays precomputed slots instead of
-// racing for them). Tokens are spread over a persistent grid sized to the SMs.
+// racing for them). A persistent grid sized to the SMs takes the tokens one at
+// a time from a work queue in the workspace (a token's cost grows with its
+// number of destinations, so a static share would leave the launch waiting on
+// its heaviest warps).
 // Lanes 0..K-1 carry the token's top-k lanes and write the small sidecar rows
 // (routing of the lanes to that destination and the source metadata).
 // This register path carries the fused cast always, and rows that travel
@@ -25,21 +28,28 @@ constexpr int kCastUnits = 4;  // 16-column units in flight per lane (cast)
 
 enum Kind { kCopyRow = 0, kCastRow = 1 };
 
+// The cast keeps more bytes in flight per warp with two CTAs per SM (up to 128
+// registers a thread) than with more, smaller-register CTAs; the row copy fits
+// four CTAs per SM.
 template <int kKind, bool kExpand, bool kAtomic = false>
-__global__ void __launch_bounds__(kCopyThreads) dispatch_kernel(DispatchArgs a) {
+__global__ void __launch_bounds__(kCopyThreads, kKind == kCastRow ? 2 : 4) dispatch_kernel(DispatchArgs a) {
   __shared__ int64_t s_row[kWarps][kMaxTopk];               // hidden destination rows
   __shared__ float s_sf[kWarps][kMaxScaleGroups];           // this token's FP8 scales
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t gwarp = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
 
-  // the next token's routing loads while this token's row streams
-  RawLane next = fetch_lane(a, gwarp, lane, kExpand, kAtomic);
-  for (int64_t tok = gwarp; tok < a.num_tokens; tok += nwarps) {
+  // tokens from the work queue; the next token's routing loads, and the one
+  // after it is taken, while this token's row streams
+  UnitStream us = start_units(gwarp, nwarps, a.num_tokens);
+  RawLane next = fetch_lane(a, us.cur, lane, kExpand, kAtomic);
+  while (us.cur < a.num_tokens) {
+    const int64_t tok = us.cur;
     const int s = static_cast<int>(tok / a.T);
     const int t = static_cast<int>(tok - static_cast<int64_t>(s) * a.T);
     const RawLane cur = next;
-    next = fetch_lane(a, tok + nwarps, lane, kExpand, kAtomic);
+    const int64_t after = take_unit(us, a.queue, lane);
+    next = fetch_lane(a, us.nxt, lane, kExpand, kAtomic);
     const TokenLanes ln = lanes_of(a, cur, tok, lane, kExpand, kAtomic);
     const int nh = hidden_rows(a, ln, lane, kExpand, s_row[warp]);
 
@@ -121,7 +131,9 @@ __global__ void __launch_bounds__(kCopyThreads) dispatch_kernel(DispatchArgs a) 
 
     write_sidecars(a, ln, s, t, lane, kExpand);
     __syncwarp();  // s_row / s_sf are rewritten by the next token
+    advance_units(us, after);
   }
+  leave_queue(us, a.queue, lane);
 
   if (kExpand && a.zero_padding)
     zero_padding_rows(a, gwarp, nwarps, lane, kKind == kCastRow || a.x_sf != nullptr);
@@ -150,10 +162,13 @@ cudaError_t launch_dispatch(const Geometry& g, const DispatchArgs& a, int num_sm
     return g.expand ? launch_one<kCastRow, true>(a, num_sms, stream)
                     : launch_one<kCastRow, false>(a, num_sms, stream);
   }
-  // Unchanged rows: bulk copies pay off once the input streams from DRAM; on small
-  // (L2-resident, latency-bound) inputs the register path has more rows in flight.
+  // Unchanged rows: bulk copies pay off once the input streams from DRAM and a
+  // row is long enough to carry the per-token work of the bulk kernel's few
+  // warps; on small (L2-resident, latency-bound) inputs, or short rows (4 KB
+  // rows, expanded: 8 writes of each), the register path has more rows in flight.
   const bool bulk = g.copy_path == 2 ||
-                    (g.copy_path == 0 && a.num_tokens * a.in_row_bytes >= kBulkAutoMinBytes);
+                    (g.copy_path == 0 && a.num_tokens * a.in_row_bytes >= kBulkAutoMinBytes &&
+                     a.in_row_bytes >= kBulkAutoMinRowBytes);
   if (bulk) return launch_dispatch_bulk(g, a, num_sms, stream);
   return g.expand ? launch_one<kCopyRow, true>(a, num_sms, stream)
                   : launch_one<kCopyRow, false>(a, num_sms, stream);

@@ -49,9 +49,10 @@ __global__ void __launch_bounds__(kBulkThreads) dispatch_bulk_kernel(DispatchArg
   }
   __syncwarp();
 
-  // pieces run (token, 0..pieces-1) for tokens gwarp, gwarp + nwarps, ...;
-  // piece i sits in stage i % 2. All lanes keep the same bookkeeping; lane 0
-  // issues the copies.
+  // pieces run (token, 0..pieces-1) for the warp's tokens (its fixed two, then
+  // those it takes from the work queue) in turn; consecutive pieces alternate
+  // between the two stages.
+  // All lanes keep the same bookkeeping; lane 0 issues the copies.
   uint32_t parity = 0;   // bit s: parity of stage s's next completion
   uint32_t pending = 0;  // bit s: a load into stage s is in flight
   auto load_piece = [&](int64_t tok, int piece, int s) {
@@ -66,20 +67,23 @@ __global__ void __launch_bounds__(kBulkThreads) dispatch_bulk_kernel(DispatchArg
 
   bool ok = true;
   int stage = 0;
-  if (gwarp < a.num_tokens) load_piece(gwarp, 0, 0);
-  RawLane next = fetch_lane(a, gwarp, lane, kExpand, false);
-  for (int64_t tok = gwarp; tok < a.num_tokens && ok; tok += nwarps) {
+  UnitStream us = start_units(gwarp, nwarps, a.num_tokens);
+  if (us.cur < a.num_tokens) load_piece(us.cur, 0, 0);
+  RawLane next = fetch_lane(a, us.cur, lane, kExpand, false);
+  while (us.cur < a.num_tokens) {
+    const int64_t tok = us.cur;
     const int s_rank = static_cast<int>(tok / a.T);
     const int t = static_cast<int>(tok - static_cast<int64_t>(s_rank) * a.T);
     const RawLane cur = next;
-    next = fetch_lane(a, tok + nwarps, lane, kExpand, false);
+    const int64_t after = take_unit(us, a.queue, lane);
+    next = fetch_lane(a, us.nxt, lane, kExpand, false);
     const TokenLanes ln = lanes_of(a, cur, tok, lane, kExpand, false);
     const int nh = hidden_rows(a, ln, lane, kExpand, s_row[warp]);
 
     for (int piece = 0; piece < pieces; ++piece) {
       // start the following piece in the other stage
       const bool last = piece + 1 == pieces;
-      const int64_t ntok = last ? tok + nwarps : tok;
+      const int64_t ntok = last ? us.nxt : tok;
       if (ntok < a.num_tokens) load_piece(ntok, last ? 0 : piece + 1, stage ^ 1);
       // store this piece to every destination row once it has landed
       int landed = 1;
@@ -110,6 +114,7 @@ __global__ void __launch_bounds__(kBulkThreads) dispatch_bulk_kernel(DispatchArg
     }
     write_sidecars(a, ln, s_rank, t, lane, kExpand);
     __syncwarp();  // s_row is rewritten by the next token
+    advance_units(us, after);
   }
 
   if (lane == 0) {
@@ -121,6 +126,7 @@ __global__ void __launch_bounds__(kBulkThreads) dispatch_bulk_kernel(DispatchArg
     if (!ok) atomicOr(a.err, kErrTimeout);
   }
   __syncwarp();
+  leave_queue(us, a.queue, lane);
 
   if (kExpand && a.zero_padding) zero_padding_rows(a, gwarp, nwarps, lane, a.x_sf != nullptr);
 }

@@ -18,6 +18,7 @@ constexpr int kCopyThreads = 256;     // dispatch / combine CTA size (8 warps)
 constexpr int kBulkThreads = 128;     // bulk-copy dispatch CTA size (4 warps)
 constexpr int kBulkStageMax = 16384;  // bytes of one shared-memory stage of the bulk-copy dispatch
 constexpr int64_t kBulkAutoMinBytes = int64_t{32} << 20;  // input rows from which copy_path 0 picks bulk
+constexpr int kBulkAutoMinRowBytes = 6144;  // and rows at least this long (shorter rows: register copies)
 constexpr int kMaxPrologueCtas = 64;
 constexpr int kMaxSortRows = 8192;   // rows of one segment the comparison sort handles
 
@@ -51,10 +52,27 @@ struct Geometry {
 
 // Byte offsets of the workspace pieces.
 struct Workspace {
-  size_t err;      // uint32: sticky device error bits
-  size_t done;     // uint32: arrival counter of the layout kernel (returns to 0)
-  size_t exp_off;  // int32 [R][E]: lanes of each expert from lower source ranks (expand)
+  size_t err;            // uint32: sticky device error bits
+  size_t done;           // uint32: arrival counter of the layout kernel (returns to 0)
+  size_t dispatch_queue; // 2 x uint64: the dispatch's work queue (returns to 0)
+  size_t combine_queue;  // 2 x uint64: the combine's work queue (returns to 0)
+  size_t exp_off;        // int32 [R][E]: lanes of each expert from lower source ranks (expand)
   size_t total;
+};
+
+// Dynamic distribution of a kernel's work units (source tokens, or token
+// column ranges) over its warps. A warp's first two units are fixed (its warp
+// index, then that plus the grid's warps); after those it takes the next unit
+// from a counter in the workspace header, so a warp that drew light tokens
+// (few destinations) takes more of them and the launch ends when the work
+// does, not when the heaviest static share does. Each take is issued one unit
+// before the warp needs it, so the atomic's round trip overlaps the current
+// unit. A launch whose units all fit the fixed part never touches the queue;
+// otherwise every warp leaves it once, and the last to leave (a second
+// counter) returns both counters to zero for the next launch.
+struct WorkQueue {
+  unsigned long long* next;
+  unsigned long long* left;
 };
 
 Workspace workspace_layout(const Geometry& g);
@@ -104,6 +122,7 @@ struct DispatchArgs {
   float* recv_w;
   int32_t* recv_md;
   uint32_t* err;             // the workspace's device error bits (null: none)
+  WorkQueue queue;           // the workspace's dispatch work queue
   int64_t recv_rows;         // rows of recv_x and recv_sf (the capacity when packed)
   int64_t side_rows;         // rows of the sidecar tensors
   int R, E, L, K, T, H, G, M, compact, zero_padding, n_so, n_su, sf_pack;
@@ -143,6 +162,7 @@ struct CombineArgs {
   const int32_t* recv_region;  // packed receive rows only
   uint16_t* out;
   uint32_t* err;     // the workspace's device error bits
+  WorkQueue queue;   // the workspace's combine work queue
   int64_t y_rows;    // rows of y (the capacity when packed)
   int E, L, K, T, H, R, M, compact;
   int splits;        // column ranges per token (work units per token)
@@ -197,6 +217,45 @@ __device__ __forceinline__ int64_t entry_row(const Args& a, int d, int slot, uin
   const int before = rb == 0 ? 0 : __ldg(a.recv_psum + d * a.R + rb - 1);
   const int64_t base = a.compact == 1 ? window : static_cast<int64_t>(__ldg(a.recv_region + d));
   return base + before + slot - static_cast<int64_t>(rb) * a.M;
+}
+
+// The units of one warp in order: `cur` is being worked on, `nxt` comes next
+// (known one unit ahead, so its routing can load during `cur`).
+struct UnitStream {
+  int64_t cur, nxt;
+  int64_t nwarps, units;
+  bool dynamic;  // units beyond the fixed two per warp come from the queue
+};
+
+__device__ __forceinline__ UnitStream start_units(int64_t gwarp, int64_t nwarps, int64_t units) {
+  return UnitStream{gwarp, gwarp + nwarps, nwarps, units, units > 2 * nwarps};
+}
+
+// Issue the take of the unit after `nxt` (all lanes get it); pass the result
+// to advance_units once the current unit is done.
+__device__ __forceinline__ int64_t take_unit(const UnitStream& u, const WorkQueue& q, int lane) {
+  if (!u.dynamic) return u.units;
+  unsigned long long v = 0;
+  if (lane == 0) v = atomicAdd(q.next, 1ull);
+  return 2 * u.nwarps + static_cast<int64_t>(__shfl_sync(0xFFFFFFFFu, v, 0));
+}
+
+__device__ __forceinline__ void advance_units(UnitStream& u, int64_t after) {
+  u.cur = u.nxt;
+  u.nxt = after;
+}
+
+// The calling warp has run out of units and is done with the queue; the last
+// of the grid's warps to leave resets it.
+__device__ __forceinline__ void leave_queue(const UnitStream& u, const WorkQueue& q, int lane) {
+  if (u.dynamic && lane == 0) {
+    __threadfence();
+    if (atomicAdd(q.left, 1ull) == static_cast<unsigned long long>(u.nwarps) - 1ull) {
+      atomicExch(q.next, 0ull);
+      atomicExch(q.left, 0ull);
+    }
+  }
+  __syncwarp();
 }
 
 // Checked builds: is row inside [0, rows)? If not, latch kErrBounds (when there

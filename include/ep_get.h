@@ -114,7 +114,8 @@ typedef struct ep_config {
   int32_t copy_path;               /* how dispatch moves rows that travel unchanged
                                       (bf16 -> bf16, pre-cast FP8): 0 = automatic
                                       (bulk copies when the input rows total
-                                      at least 32 MiB, register copies below);
+                                      at least 32 MiB and a row is at least 6 KB,
+                                      register copies otherwise);
                                       1 = 16-byte register loads and stores; 2 = bulk
                                       copies through shared memory. Results never
                                       depend on it; the fused cast ignores it.     */
@@ -188,9 +189,12 @@ typedef struct ep_recv {
 
 /* Workspace bytes the three entry points need for this configuration (the
  * library's own convention: the pages' buffers are transport windows with no
- * single-GPU counterpart). The workspace must be zero-filled before its first
- * use (ep_workspace_init or a zeroing allocator); afterwards the library keeps
- * it consistent. One workspace serves one stream at a time. */
+ * single-GPU counterpart): a 256-byte header (the device error word, the
+ * layout's arrival counter, and the work queues from which the dispatch and
+ * combine warps take their tokens), plus per-(source, expert) offsets when
+ * expanding. The workspace must be zero-filled before its first use
+ * (ep_workspace_init or a zeroing allocator); afterwards every kernel returns
+ * its counters to zero itself. One workspace serves one stream at a time. */
 size_t ep_workspace_bytes(const ep_config_t* cfg);
 
 /* Rows the receive buffer recv_x needs: R*R*M (row form and compact; the
@@ -283,10 +287,11 @@ int ep_combine(const ep_config_t* cfg, const ep_layout_t* layout, const uint16_t
  * ep_dispatch_atomic: ep_dispatch without a layout. send_counters: device int32
  * [R src][R dst], zeroed on `stream` by the call, then left holding how many
  * rows each source sent each destination. Rows land in the source's row block
- * of the destination region in race order. */
+ * of the destination region in race order. The workspace (as for ep_dispatch)
+ * carries the work queue that spreads the tokens over the warps. */
 int ep_dispatch_atomic(const ep_config_t* cfg, const void* x, const float* x_sf,
                        const int64_t* topk_idx, const float* topk_weights, const ep_recv_t* recv,
-                       int32_t* send_counters, void* stream);
+                       int32_t* send_counters, void* workspace, size_t workspace_bytes, void* stream);
 
 /* ep_deterministic_sort: sorts every (destination, row block) segment of `recv`
  * (filled by ep_dispatch_atomic; the sidecars must be present: the key is the

@@ -311,7 +311,7 @@ def test_atomic_slots_plus_sort_equal_the_deterministic_dispatch(name):
     det = GpuRun(wl, idx, w, x, sf).layout().dispatch()
     racy = ep.alloc_recv(det.cfg, det.dev, zero=True)
     counters = torch.full((wl.num_ranks, wl.num_ranks), 7, dtype=torch.int32, device=det.dev)
-    ep.ep_dispatch_atomic(det.cfg, det.x, det.sf, det.idx, det.w, racy, counters)
+    ep.ep_dispatch_atomic(det.cfg, det.x, det.sf, det.idx, det.w, racy, counters, det.ws)
     assert torch.equal(counters, det.lay.num_tokens_per_rank)
     srt = ep.alloc_recv(det.cfg, det.dev, zero=True)
     ep.ep_deterministic_sort(det.cfg, racy, counters, srt)
@@ -397,3 +397,22 @@ def test_packed_capacity_overflow_is_reported(name):
     st, o_out = oracle.combine(wl, olay, u16(y), idx, w)
     assert st == oracle.OVERFLOW
     assert np.array_equal(u16(run.out), o_out)
+
+
+def test_work_queues_return_to_zero():
+    """Dispatch and combine warps take their tokens from counters in the
+    workspace header; after every launch, whatever the grid, the last warp to
+    leave has put them back to zero (and the results never depend on the grid)."""
+    wl = W.PARITY["direct_zipf"]
+    idx, w, x, sf = inputs(wl)
+    ref = None
+    for sms, path in ((0, 1), (1, 2), (5, 1), (152, 2), (0, 2)):
+        run = GpuRun(wl, idx, w, x, sf, num_sms=sms, copy_path=path).layout().dispatch()
+        run.combine(run.recv.recv_x)
+        assert run.status() == ep.EP_OK
+        header = run.ws[:256].cpu().numpy()
+        assert not header[4:40].any(), header[:40]
+        got = (u16(run.recv.recv_x), u16(run.out))
+        if ref is None:
+            ref = got
+        assert np.array_equal(got[0], ref[0]) and np.array_equal(got[1], ref[1])
