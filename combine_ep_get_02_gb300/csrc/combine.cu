@@ -26,11 +26,12 @@ __global__ void __launch_bounds__(kCopyThreads) combine_kernel(CombineArgs a) {
 
   // A work unit is one token's column range (a token is split into a.splits
   // ranges of a.split_chunks 16-byte chunks when tokens are too few to keep
-  // every warp busy to the end). Warps take units from the workspace's work
-  // queue (a token's cost grows with its number of valid lanes). Lane k of the
-  // warp carries top-k lane k of the unit's token; the next unit is taken, and
-  // its routing (expert, slot or position, weight) loaded, while the current
-  // unit's rows stream.
+  // every warp busy to the end). In the row form warps take units from the
+  // workspace's work queue (a token's cost follows its number of distinct
+  // rows); expanded units keep a fixed share. Lane k of the warp carries top-k
+  // lane k of the unit's token; the next unit is taken, and its routing
+  // (expert, slot or position, weight) loaded, while the current unit's rows
+  // stream.
   const int64_t units = a.num_tokens * a.splits;
   int64_t e_next = -1;
   int r_next = -1;
@@ -47,7 +48,7 @@ __global__ void __launch_bounds__(kCopyThreads) combine_kernel(CombineArgs a) {
     }
   };
   const int64_t gwarp = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
-  UnitStream us = start_units(gwarp, nwarps, units);
+  UnitStream us = start_units(gwarp, nwarps, units, !kExpand);
   load_raw(us.cur);
   while (us.cur < units) {
     const int64_t unit = us.cur;

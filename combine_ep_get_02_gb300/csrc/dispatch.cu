@@ -5,10 +5,10 @@
 // loads, each lane a strided set of chunks), optionally casts it to FP8-e4m3
 // in registers, and stores it to each destination row; the slots come from the
 // layout (PR #753, Approach: the kernel replays precomputed slots instead of
-// racing for them). A persistent grid sized to the SMs takes the tokens one at
-// a time from a work queue in the workspace (a token's cost grows with its
-// number of destinations, so a static share would leave the launch waiting on
-// its heaviest warps).
+// racing for them). A persistent grid sized to the SMs works through the
+// tokens; in the row form it takes them from a work queue in the workspace (a
+// token's cost grows with its number of destinations, so a static share would
+// leave the launch waiting on its heaviest warps).
 // Lanes 0..K-1 carry the token's top-k lanes and write the small sidecar rows
 // (routing of the lanes to that destination and the source metadata).
 // This register path carries the fused cast always, and rows that travel
@@ -41,7 +41,7 @@ __global__ void __launch_bounds__(kCopyThreads, kKind == kCastRow ? 2 : 4) dispa
 
   // tokens from the work queue; the next token's routing loads, and the one
   // after it is taken, while this token's row streams
-  UnitStream us = start_units(gwarp, nwarps, a.num_tokens);
+  UnitStream us = start_units(gwarp, nwarps, a.num_tokens, !kExpand);
   RawLane next = fetch_lane(a, us.cur, lane, kExpand, kAtomic);
   while (us.cur < a.num_tokens) {
     const int64_t tok = us.cur;
@@ -162,13 +162,10 @@ cudaError_t launch_dispatch(const Geometry& g, const DispatchArgs& a, int num_sm
     return g.expand ? launch_one<kCastRow, true>(a, num_sms, stream)
                     : launch_one<kCastRow, false>(a, num_sms, stream);
   }
-  // Unchanged rows: bulk copies pay off once the input streams from DRAM and a
-  // row is long enough to carry the per-token work of the bulk kernel's few
-  // warps; on small (L2-resident, latency-bound) inputs, or short rows (4 KB
-  // rows, expanded: 8 writes of each), the register path has more rows in flight.
+  // Unchanged rows: bulk copies pay off once the input streams from DRAM; on small
+  // (L2-resident, latency-bound) inputs the register path has more rows in flight.
   const bool bulk = g.copy_path == 2 ||
-                    (g.copy_path == 0 && a.num_tokens * a.in_row_bytes >= kBulkAutoMinBytes &&
-                     a.in_row_bytes >= kBulkAutoMinRowBytes);
+                    (g.copy_path == 0 && a.num_tokens * a.in_row_bytes >= kBulkAutoMinBytes);
   if (bulk) return launch_dispatch_bulk(g, a, num_sms, stream);
   return g.expand ? launch_one<kCopyRow, true>(a, num_sms, stream)
                   : launch_one<kCopyRow, false>(a, num_sms, stream);

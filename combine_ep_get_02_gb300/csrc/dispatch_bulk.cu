@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(kBulkThreads) dispatch_bulk_kernel(DispatchArg
 
   bool ok = true;
   int stage = 0;
-  UnitStream us = start_units(gwarp, nwarps, a.num_tokens);
+  UnitStream us = start_units(gwarp, nwarps, a.num_tokens, !kExpand);
   if (us.cur < a.num_tokens) load_piece(us.cur, 0, 0);
   RawLane next = fetch_lane(a, us.cur, lane, kExpand, false);
   while (us.cur < a.num_tokens) {

@@ -136,43 +136,89 @@ __device__ __forceinline__ CastUnit cast_unit(const uint4& lo, const uint4& hi, 
   return c;
 }
 
+// Sidecar rows of a token with top-k <= 8, all entries at once: lanes 4i..4i+3
+// write entry i (the i-th deduplicated destination, in lane order), each lane
+// two of its K routing values and three of its 2 + K metadata fields; the
+// token's lanes' experts, destinations, weights and positions come by shuffle.
+__device__ __forceinline__ void write_sidecars_k8(const DispatchArgs& a, const TokenLanes& ln, int s, int t,
+                                                  int lane, bool kExpand) {
+  const int K = a.K;
+  const int n = __popc(ln.rmask);
+  const int i = lane >> 2, q = lane & 3;
+  const bool active = i < n;
+  const int ri = active ? static_cast<int>(__fns(ln.rmask, 0, i + 1)) : 0;  // lane of entry i
+  const int di = __shfl_sync(kFullMask, ln.d, ri);
+  const int64_t mrow = __shfl_sync(kFullMask, ln.row, ri);
+  // packed rows past the capacity (and, checked builds, rows outside the
+  // buffer) are skipped; one lane per entry reports it
+  const bool ok = active && row_usable(mrow, a.side_rows, a.compact == 2, q == 0 ? a.err : nullptr);
+  const int k0 = 2 * q, k1 = 2 * q + 1;
+  const int e0 = __shfl_sync(kFullMask, ln.e, k0), e1 = __shfl_sync(kFullMask, ln.e, k1);
+  const int d0 = __shfl_sync(kFullMask, ln.d, k0), d1 = __shfl_sync(kFullMask, ln.d, k1);
+  const float w0 = __shfl_sync(kFullMask, ln.w, k0), w1 = __shfl_sync(kFullMask, ln.w, k1);
+  if (ok && a.recv_idx) {
+    int64_t* r = a.recv_idx + mrow * K;
+    if (k0 < K) r[k0] = d0 == di ? static_cast<int64_t>(e0 - di * a.L) : -1;
+    if (k1 < K) r[k1] = d1 == di ? static_cast<int64_t>(e1 - di * a.L) : -1;
+  }
+  if (ok && a.recv_w) {
+    float* r = a.recv_w + mrow * K;
+    if (k0 < K) r[k0] = d0 == di ? w0 : 0.f;
+    if (k1 < K) r[k1] = d1 == di ? w1 : 0.f;
+  }
+  if (a.recv_md) {
+    int32_t* md = a.recv_md + mrow * (K + 2);
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+      const int f = q + 4 * j;  // field f = 2 + k carries lane k's expanded row
+      const int src = (f - 2) & 31;
+      const int dk = __shfl_sync(kFullMask, ln.d, src);
+      const int pk = kExpand ? __shfl_sync(kFullMask, ln.pos, src) : -1;
+      if (ok && f < K + 2) md[f] = f == 0 ? s : (f == 1 ? t : ((kExpand && dk == di) ? pk : -1));
+    }
+  }
+}
+
 // Sidecar rows of each deduplicated destination of a token (row form): the
 // routing of the lanes to that destination and the source metadata.
 __device__ __forceinline__ void write_sidecars(const DispatchArgs& a, const TokenLanes& ln, int s, int t,
                                                int lane, bool kExpand) {
-  // sidecar rows of each deduplicated destination (row form). Metadata field
+  if (a.recv_idx == nullptr && a.recv_w == nullptr && a.recv_md == nullptr) return;
+  if (a.K <= 8) {
+    write_sidecars_k8(a, ln, s, t, lane, kExpand);
+    return;
+  }
+  // top-k above 8: one deduplicated destination at a time. Metadata field
   // f = 2 + k carries lane k's expanded row; with K up to 32 there are up to 34
   // fields, so a lane writes fields lane and lane + 32.
-  if (a.recv_idx != nullptr || a.recv_w != nullptr || a.recv_md != nullptr) {
-    const int f0_d = __shfl_sync(kFullMask, ln.d, (lane - 2) & 31);   // lane f-2 for f = lane
-    const int f0_pos = __shfl_sync(kFullMask, ln.pos, (lane - 2) & 31);
-    const int f1_d = __shfl_sync(kFullMask, ln.d, (lane + 30) & 31);  // f = lane + 32
-    const int f1_pos = __shfl_sync(kFullMask, ln.pos, (lane + 30) & 31);
-    unsigned m = ln.rmask;
-    while (m) {
-      const int rl = __ffs(m) - 1;
-      m &= m - 1;
-      const int dj = __shfl_sync(kFullMask, ln.d, rl);
-      const int64_t mrow = __shfl_sync(kFullMask, ln.row, rl);
-      // packed rows past the capacity (and, checked builds, rows outside the
-      // buffer) are skipped; the same for every lane
-      if (!row_usable(mrow, a.side_rows, a.compact == 2, lane == 0 ? a.err : nullptr)) continue;
-      if (lane < a.K) {
-        const bool on = ln.d == dj;
-        if (a.recv_idx) a.recv_idx[mrow * a.K + lane] = on ? static_cast<int64_t>(ln.e - dj * a.L) : -1;
-        if (a.recv_w) a.recv_w[mrow * a.K + lane] = on ? ln.w : 0.f;
+  const int f0_d = __shfl_sync(kFullMask, ln.d, (lane - 2) & 31);   // lane f-2 for f = lane
+  const int f0_pos = __shfl_sync(kFullMask, ln.pos, (lane - 2) & 31);
+  const int f1_d = __shfl_sync(kFullMask, ln.d, (lane + 30) & 31);  // f = lane + 32
+  const int f1_pos = __shfl_sync(kFullMask, ln.pos, (lane + 30) & 31);
+  unsigned m = ln.rmask;
+  while (m) {
+    const int rl = __ffs(m) - 1;
+    m &= m - 1;
+    const int dj = __shfl_sync(kFullMask, ln.d, rl);
+    const int64_t mrow = __shfl_sync(kFullMask, ln.row, rl);
+    // packed rows past the capacity (and, checked builds, rows outside the
+    // buffer) are skipped; the same for every lane
+    if (!row_usable(mrow, a.side_rows, a.compact == 2, lane == 0 ? a.err : nullptr)) continue;
+    if (lane < a.K) {
+      const bool on = ln.d == dj;
+      if (a.recv_idx) a.recv_idx[mrow * a.K + lane] = on ? static_cast<int64_t>(ln.e - dj * a.L) : -1;
+      if (a.recv_w) a.recv_w[mrow * a.K + lane] = on ? ln.w : 0.f;
+    }
+    if (a.recv_md) {
+      int32_t* md = a.recv_md + mrow * (a.K + 2);
+      if (lane < a.K + 2) {
+        int v;
+        if (lane == 0) v = s;
+        else if (lane == 1) v = t;
+        else v = (kExpand && f0_d == dj) ? f0_pos : -1;
+        md[lane] = v;
       }
-      if (a.recv_md) {
-        int32_t* md = a.recv_md + mrow * (a.K + 2);
-        if (lane < a.K + 2) {
-          int v;
-          if (lane == 0) v = s;
-          else if (lane == 1) v = t;
-          else v = (kExpand && f0_d == dj) ? f0_pos : -1;
-          md[lane] = v;
-        }
-        if (lane + 32 < a.K + 2) md[lane + 32] = (kExpand && f1_d == dj) ? f1_pos : -1;
-      }
+      if (lane + 32 < a.K + 2) md[lane + 32] = (kExpand && f1_d == dj) ? f1_pos : -1;
     }
   }
 }

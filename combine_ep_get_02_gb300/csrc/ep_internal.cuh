@@ -9,6 +9,7 @@
 namespace ep {
 
 constexpr int kLayoutThreads = 256;  // one thread per token in the layout kernels
+constexpr int kRowsThreads = 256;    // the row-form layout kernel's CTA
 constexpr int kLayoutWarps = kLayoutThreads / 32;
 constexpr int kMaxRanks = 64;
 constexpr int kMaxTopk = 32;
@@ -18,7 +19,6 @@ constexpr int kCopyThreads = 256;     // dispatch / combine CTA size (8 warps)
 constexpr int kBulkThreads = 128;     // bulk-copy dispatch CTA size (4 warps)
 constexpr int kBulkStageMax = 16384;  // bytes of one shared-memory stage of the bulk-copy dispatch
 constexpr int64_t kBulkAutoMinBytes = int64_t{32} << 20;  // input rows from which copy_path 0 picks bulk
-constexpr int kBulkAutoMinRowBytes = 6144;  // and rows at least this long (shorter rows: register copies)
 constexpr int kMaxPrologueCtas = 64;
 constexpr int kMaxSortRows = 8192;   // rows of one segment the comparison sort handles
 
@@ -61,15 +61,16 @@ struct Workspace {
 };
 
 // Dynamic distribution of a kernel's work units (source tokens, or token
-// column ranges) over its warps. A warp's first two units are fixed (its warp
-// index, then that plus the grid's warps); after those it takes the next unit
-// from a counter in the workspace header, so a warp that drew light tokens
-// (few destinations) takes more of them and the launch ends when the work
-// does, not when the heaviest static share does. Each take is issued one unit
-// before the warp needs it, so the atomic's round trip overlaps the current
-// unit. A launch whose units all fit the fixed part never touches the queue;
-// otherwise every warp leaves it once, and the last to leave (a second
-// counter) returns both counters to zero for the next launch.
+// column ranges) over its warps. In the row form a token's cost follows its
+// number of distinct destinations (1 to min(K, R)), so a fixed share per warp
+// leaves the launch waiting on its heaviest warps; there a warp's first two
+// units are fixed (its warp index, then that plus the grid's warps) and after
+// those it takes the next unit from a counter in the workspace header. Each
+// take is issued one unit before the warp needs it, so the atomic's round trip
+// overlaps the current unit. Every warp leaves the queue once, and the last to
+// leave (a second counter) returns both counters to zero for the next launch.
+// Expanded tokens all carry about K rows; they keep the fixed share (units
+// gwarp, gwarp + nwarps, ...), as does a launch whose units fit two per warp.
 struct WorkQueue {
   unsigned long long* next;
   unsigned long long* left;
@@ -227,14 +228,14 @@ struct UnitStream {
   bool dynamic;  // units beyond the fixed two per warp come from the queue
 };
 
-__device__ __forceinline__ UnitStream start_units(int64_t gwarp, int64_t nwarps, int64_t units) {
-  return UnitStream{gwarp, gwarp + nwarps, nwarps, units, units > 2 * nwarps};
+__device__ __forceinline__ UnitStream start_units(int64_t gwarp, int64_t nwarps, int64_t units, bool queue) {
+  return UnitStream{gwarp, gwarp + nwarps, nwarps, units, queue && units > 2 * nwarps};
 }
 
 // Issue the take of the unit after `nxt` (all lanes get it); pass the result
 // to advance_units once the current unit is done.
 __device__ __forceinline__ int64_t take_unit(const UnitStream& u, const WorkQueue& q, int lane) {
-  if (!u.dynamic) return u.units;
+  if (!u.dynamic) return u.nxt + u.nwarps;  // the fixed share
   unsigned long long v = 0;
   if (lane == 0) v = atomicAdd(q.next, 1ull);
   return 2 * u.nwarps + static_cast<int64_t>(__shfl_sync(0xFFFFFFFFu, v, 0));

@@ -120,6 +120,64 @@ __device__ __forceinline__ uint64_t load_token(const LayoutArgs& a, int64_t tok,
   return dmask;
 }
 
+// The end of every layout CTA: count it in; the last CTA of the grid turns the
+// receive counts (recv_cnt, published by each source's last CTA, fenced
+// before this) into their prefix sums over the row blocks and the first
+// packed row of each destination, then returns the counter to zero.
+template <int THREADS>
+__device__ __forceinline__ void finish_receive_sums(const LayoutArgs& a, int32_t* s_cnt, int32_t* s_tot,
+                                                    bool* s_last) {
+  constexpr int WARPS = THREADS / 32;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int R = a.R;
+  if (tid == 0) *s_last = atomicAdd(a.done, 1u) == gridDim.x - 1u;
+  __syncthreads();
+  if (!*s_last) return;
+  __threadfence();
+  for (int i = tid; i < R * R; i += THREADS) s_cnt[i] = ld_cg(a.recv_cnt + i);
+  __syncthreads();
+  // one warp per destination: inclusive scan over the row blocks, 32 at a time
+  for (int d = warp; d < R; d += WARPS) {
+    int carry = 0;
+    for (int i0 = 0; i0 < R; i0 += 32) {
+      const int i = i0 + lane;  // row block i holds source src(i)
+      int v = 0;
+      if (i < R) v = s_cnt[d * R + (a.n_so == 1 ? i : (i % a.n_so) * a.n_su + i / a.n_so)];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(kFullMask, v, o);
+        if (lane >= o) v += u;
+      }
+      v += carry;
+      if (i < R) a.recv_psum[d * R + i] = v;
+      carry = __shfl_sync(kFullMask, v, 31);
+    }
+    if (lane == 0) s_tot[d] = carry;
+  }
+  // packed receive rows: destination d starts after everything the
+  // destinations before it receive
+  if (a.recv_region != nullptr) {
+    __syncthreads();
+    if (warp == 0) {
+      int carry = 0;
+      for (int d0 = 0; d0 < R; d0 += 32) {
+        const int d = d0 + lane;
+        const int n = d < R ? s_tot[d] : 0;
+        int v = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int u = __shfl_up_sync(kFullMask, v, o);
+          if (lane >= o) v += u;
+        }
+        if (d < R) a.recv_region[d] = carry + v - n;
+        carry += __shfl_sync(kFullMask, v, 31);
+      }
+      if (lane == 0) a.recv_region[R] = carry;
+    }
+  }
+  if (tid == 0) *a.done = 0u;  // ready for the next call
+}
+
 }  // namespace
 
 // dynamic shared memory: cnt_e [E] | run_e [E] (expand) | ebits [WARPS][E] (expand)
@@ -329,55 +387,159 @@ __global__ void __launch_bounds__(THREADS) layout_kernel(LayoutArgs a) {
     }
   }
 
-  // ---- the last CTA of the grid: prefix sums of the receive counts
   __threadfence();
   cluster.barrier_wait();
-  if (tid == 0) s_last = atomicAdd(a.done, 1u) == gridDim.x - 1u;
+  finish_receive_sums<THREADS>(a, s_cnt, s_tot, &s_last);
+}
+
+// Row form (no expanded positions) with top-k <= 8: the same counts, scan and
+// slots as layout_kernel, reorganised for latency. Each CTA (256 threads) holds
+// every round of its tokens' lanes in registers and, in pass 1, records each
+// (round, warp)'s token count per destination; after the cluster scan one
+// barrier turns those counts into every (round, warp)'s base, so pass 2 runs
+// without barriers: a lane's rank among its warp's tokens to destination d is
+// the popcount below it of column d of the warp's destination bit matrix
+// (fetched from lane d with a shuffle).
+template <int ROUNDS>
+__global__ void __launch_bounds__(kRowsThreads) layout_rows_kernel(LayoutArgs a) {
+  constexpr int THREADS = kRowsThreads, WARPS = THREADS / 32, KMAX = 8;
+  cg::cluster_group cluster = cg::this_cluster();
+  extern __shared__ int32_t smem[];
+  int32_t* cnt_e = smem;  // [E]
+  __shared__ int32_t cnt_d[kMaxRanks];
+  __shared__ int32_t wcnt[ROUNDS * WARPS][kMaxRanks];  // counts of each (round, warp), then their bases
+  __shared__ int32_t s_cnt[kMaxRanks * kMaxRanks];
+  __shared__ int32_t s_tot[kMaxRanks];
+  __shared__ bool s_last;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const unsigned lt = lanemask_lt();
+  const int R = a.R, E = a.E;
+  const int s = blockIdx.x / a.C;
+  const int c = static_cast<int>(cluster.block_rank());
+  const int t_begin = min(a.T, c * a.TB), t_end = min(a.T, t_begin + a.TB);
+  const int64_t tok_base = static_cast<int64_t>(s) * a.T;
+
+  for (int e = tid; e < E; e += THREADS) cnt_e[e] = 0;
   __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  for (int i = tid; i < R * R; i += THREADS) s_cnt[i] = ld_cg(a.recv_cnt + i);
-  __syncthreads();
-  // one warp per destination: inclusive scan over the row blocks, 32 at a time
-  for (int d = warp; d < R; d += WARPS) {
-    int carry = 0;
-    for (int i0 = 0; i0 < R; i0 += 32) {
-      const int i = i0 + lane;  // row block i holds source src(i)
-      int v = 0;
-      if (i < R) v = s_cnt[d * R + (a.n_so == 1 ? i : (i % a.n_so) * a.n_su + i / a.n_so)];
+
+  // ---- pass 1: every round's lanes at once, counted per expert and per
+  // (round, warp, destination)
+  bool bad = false;
+  int e[ROUNDS][KMAX];
+  uint64_t dmask[ROUNDS];
+  uint32_t col_lo[ROUNDS], col_hi[ROUNDS];
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int u = __shfl_up_sync(kFullMask, v, o);
-        if (lane >= o) v += u;
-      }
-      v += carry;
-      if (i < R) a.recv_psum[d * R + i] = v;
-      carry = __shfl_sync(kFullMask, v, 31);
-    }
-    if (lane == 0) s_tot[d] = carry;
+  for (int r = 0; r < ROUNDS; ++r) {
+    const int t = t_begin + r * THREADS + tid;
+    dmask[r] = load_token<KMAX>(a, tok_base + t, t < t_end, e[r], &bad);
   }
-  // packed receive rows: destination d starts after everything the
-  // destinations before it receive
-  if (a.recv_region != nullptr) {
-    __syncthreads();
-    if (warp == 0) {
-      int carry = 0;
-      for (int d0 = 0; d0 < R; d0 += 32) {
-        const int d = d0 + lane;
-        const int n = d < R ? s_tot[d] : 0;
-        int v = n;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int u = __shfl_up_sync(kFullMask, v, o);
-          if (lane >= o) v += u;
+  for (int r = 0; r < ROUNDS; ++r) {
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k)
+      if (e[r][k] >= 0) atomicAdd(&cnt_e[e[r][k]], 1);
+    // lane d: the warp's tokens that reach destination d (and d + 32)
+    col_lo[r] = warp_transpose32(static_cast<uint32_t>(dmask[r]), lane);
+    if (lane < R) wcnt[r * WARPS + warp][lane] = __popc(col_lo[r]);
+    col_hi[r] = 0;
+    if (R > 32) {
+      col_hi[r] = warp_transpose32(static_cast<uint32_t>(dmask[r] >> 32), lane);
+      if (lane + 32 < R) wcnt[r * WARPS + warp][lane + 32] = __popc(col_hi[r]);
+    }
+  }
+  if (bad) atomicOr(a.err, kErrBadTopk);
+  __syncthreads();
+  for (int d = tid; d < R; d += THREADS) {
+    int n = 0;
+#pragma unroll
+    for (int rw = 0; rw < ROUNDS * WARPS; ++rw) n += wcnt[rw][d];
+    cnt_d[d] = n;
+  }
+  cluster.sync();
+
+  // ---- scan across the cluster: counts of the CTAs before this one; this
+  // CTA's (round, warp) counts become their bases
+  const int rb = row_block(s, a.n_so, a.n_su);
+  for (int d = tid; d < R; d += THREADS) {
+    int base = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (q < c) base += cluster.map_shared_rank(cnt_d, q)[d];
+    if (c == a.C - 1) {  // the source's totals
+      const int total = base + cnt_d[d];
+      a.num_tokens_per_rank[s * R + d] = total;
+      a.recv_cnt[d * R + s] = total;
+    }
+    int run = rb * a.M + base;
+#pragma unroll
+    for (int rw = 0; rw < ROUNDS * WARPS; ++rw) {
+      const int n = wcnt[rw][d];
+      wcnt[rw][d] = run;
+      run += n;
+    }
+  }
+  for (int x = tid; x < E; x += THREADS) {
+    int base = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (q < c) base += cluster.map_shared_rank(cnt_e, q)[x];
+    if (c == a.C - 1) a.num_tokens_per_expert[s * E + x] = base + cnt_e[x];
+  }
+  // other CTAs may still read this CTA's counts: they are left untouched, and
+  // the CTA waits for the whole cluster before it exits
+  cluster.barrier_arrive();
+  __syncthreads();
+
+  // ---- pass 2: slots, no barriers
+#pragma unroll
+  for (int r = 0; r < ROUNDS; ++r) {
+    const int t = t_begin + r * THREADS + tid;
+    int slot[KMAX];
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) {
+      const int d = e[r][k] >= 0 ? div_l(e[r][k], a.l_magic) : 0;
+      uint32_t col = __shfl_sync(kFullMask, col_lo[r], d & 31);  // every lane takes part
+      if (R > 32) {
+        const uint32_t hi = __shfl_sync(kFullMask, col_hi[r], d & 31);
+        if (d >= 32) col = hi;
+      }
+      slot[k] = -1;
+      if (e[r][k] >= 0) {
+        slot[k] = wcnt[r * WARPS + warp][d] + __popc(col & lt);
+        // checked builds: the slot stays inside this source's row block
+        if (!row_in_bounds(slot[k] - static_cast<int64_t>(rb) * a.M, a.M, a.err)) slot[k] = -1;
+      }
+    }
+    if (t < t_end) {
+      const int64_t tok = tok_base + t;
+      int32_t* srow = a.slot_map + tok * a.K;
+      if (a.K == KMAX && aligned16(srow)) {
+        *reinterpret_cast<int4*>(srow) = make_int4(slot[0], slot[1], slot[2], slot[3]);
+        *reinterpret_cast<int4*>(srow + 4) = make_int4(slot[4], slot[5], slot[6], slot[7]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < KMAX; ++k)
+          if (k < a.K) srow[k] = slot[k];
+      }
+      uint8_t* row = a.is_token_in_rank + tok * R;
+      if ((R & 3) == 0) {
+        for (int d = 0; d < R; d += 4) {
+          const uint32_t v = static_cast<uint32_t>((dmask[r] >> d) & 1) |
+                             static_cast<uint32_t>((dmask[r] >> (d + 1)) & 1) << 8 |
+                             static_cast<uint32_t>((dmask[r] >> (d + 2)) & 1) << 16 |
+                             static_cast<uint32_t>((dmask[r] >> (d + 3)) & 1) << 24;
+          *reinterpret_cast<uint32_t*>(row + d) = v;
         }
-        if (d < R) a.recv_region[d] = carry + v - n;
-        carry += __shfl_sync(kFullMask, v, 31);
+      } else {
+        for (int d = 0; d < R; ++d) row[d] = static_cast<uint8_t>((dmask[r] >> d) & 1);
       }
-      if (lane == 0) a.recv_region[R] = carry;
     }
   }
-  if (tid == 0) *a.done = 0u;  // ready for the next call
+
+  __threadfence();
+  cluster.barrier_wait();
+  finish_receive_sums<THREADS>(a, s_cnt, s_tot, &s_last);
 }
 
 // Expanded layout, step 2: for 32 experts per CTA, the exclusive prefix of the
@@ -478,19 +640,18 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_expand_kernel(LayoutArg
 
 namespace {
 
-template <int KMAX, int THREADS>
-cudaError_t launch_main(const Geometry& g, const LayoutArgs& a, cudaStream_t stream) {
-  const size_t smem = sizeof(int32_t) * g.E +
-                      (g.expand ? sizeof(int32_t) * (g.E + static_cast<size_t>(THREADS / 32) * g.E) : 0);
+// One thread-block cluster of a.C CTAs per source rank.
+template <typename Kernel>
+cudaError_t launch_clusters(Kernel kernel, const Geometry& g, const LayoutArgs& a, int threads, size_t smem,
+                            cudaStream_t stream) {
   cudaError_t err;
   if (smem > 32 * 1024 &&
-      (err = cudaFuncSetAttribute(layout_kernel<KMAX, THREADS>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  static_cast<int>(smem))) != cudaSuccess)
+      (err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem))) !=
+          cudaSuccess)
     return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(g.R * a.C));
-  cfg.blockDim = dim3(THREADS);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -500,7 +661,14 @@ cudaError_t launch_main(const Geometry& g, const LayoutArgs& a, cudaStream_t str
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, layout_kernel<KMAX, THREADS>, a);
+  return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
+template <int KMAX, int THREADS>
+cudaError_t launch_main(const Geometry& g, const LayoutArgs& a, cudaStream_t stream) {
+  const size_t smem = sizeof(int32_t) * g.E +
+                      (g.expand ? sizeof(int32_t) * (g.E + static_cast<size_t>(THREADS / 32) * g.E) : 0);
+  return launch_clusters(layout_kernel<KMAX, THREADS>, g, a, THREADS, smem, stream);
 }
 
 }  // namespace
@@ -508,12 +676,16 @@ cudaError_t launch_main(const Geometry& g, const LayoutArgs& a, cudaStream_t str
 cudaError_t launch_layout(const Geometry& g, const LayoutArgs& args, int num_prologue_sms,
                           cudaStream_t stream) {
   LayoutArgs a = args;
-  // one thread per token: 512-thread CTAs (256 when expanding, whose per-warp
-  // expert bitmaps take shared memory), as many CTAs per source as one round
-  // each needs, at most 8 (a portable cluster), within the prologue budget of
-  // 2 CTAs per requested SM and at least one CTA per source
-  // (top-k above 8 also takes 256: 32 lanes a token do not fit 512 threads' registers)
-  const int threads = (g.expand || g.K > 8) ? 256 : 512;
+  // One thread per token and round. Row form with top-k <= 8: 256-thread CTAs,
+  // as many per source as make rounds of 256 tokens, at most 8 (a portable
+  // cluster; on GB300 a 16th cluster of 512-thread CTAs started about 7 us after
+  // the others), each holding up to four rounds in registers. Otherwise (the
+  // expanded layout, whose per-warp expert bitmaps take shared memory, or
+  // top-k above 8, whose lanes do not fit 512 threads' registers) 256-thread
+  // CTAs of the general kernel. Always within the prologue budget of 2 CTAs per
+  // requested SM, and at least one CTA per source.
+  const bool rows = !g.expand && g.K <= 8;
+  const int threads = rows ? kRowsThreads : 256;
   const int sms = num_prologue_sms > 0 ? (num_prologue_sms < kMaxPrologueCtas ? num_prologue_sms
                                                                                : kMaxPrologueCtas)
                                        : kMaxPrologueCtas;
@@ -524,11 +696,17 @@ cudaError_t launch_layout(const Geometry& g, const LayoutArgs& args, int num_pro
   a.C = C;
   a.TB = (g.T + C - 1) / C;
   a.l_magic = g.L == 1 ? 0u : static_cast<uint32_t>((0x100000000ull + g.L - 1) / g.L);
+  const int rounds = (a.TB + threads - 1) / threads;
+  const size_t smem_rows = sizeof(int32_t) * g.E;
   cudaError_t err;
-  if (g.expand)
-    err = g.K <= 8 ? launch_main<8, 256>(g, a, stream) : launch_main<32, 256>(g, a, stream);
+  if (rows && rounds <= 1)
+    err = launch_clusters(layout_rows_kernel<1>, g, a, threads, smem_rows, stream);
+  else if (rows && rounds <= 2)
+    err = launch_clusters(layout_rows_kernel<2>, g, a, threads, smem_rows, stream);
+  else if (rows && rounds <= 4)
+    err = launch_clusters(layout_rows_kernel<4>, g, a, threads, smem_rows, stream);
   else
-    err = g.K <= 8 ? launch_main<8, 512>(g, a, stream) : launch_main<32, 256>(g, a, stream);
+    err = g.K <= 8 ? launch_main<8, 256>(g, a, stream) : launch_main<32, 256>(g, a, stream);
   if (err != cudaSuccess) return err;
   if (g.expand) {
     layout_expert_scan_kernel<<<(g.E + 31) / 32, kLayoutThreads, 0, stream>>>(a);

@@ -114,8 +114,7 @@ typedef struct ep_config {
   int32_t copy_path;               /* how dispatch moves rows that travel unchanged
                                       (bf16 -> bf16, pre-cast FP8): 0 = automatic
                                       (bulk copies when the input rows total
-                                      at least 32 MiB and a row is at least 6 KB,
-                                      register copies otherwise);
+                                      at least 32 MiB, register copies below);
                                       1 = 16-byte register loads and stores; 2 = bulk
                                       copies through shared memory. Results never
                                       depend on it; the fused cast ignores it.     */
