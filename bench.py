@@ -338,17 +338,25 @@ def native(args):
         torch.cuda.synchronize(dev)
         t_start.record(stream)
         for i in range(args.steps):
-            step(ev[i])
+            step()
         t_end.record(stream)
         torch.cuda.synchronize(dev)
         barrier(world)
     total_ms = t_start.elapsed_time(t_end)
     total_ms = max_over_ranks(world, total_ms)
     ms_per_step = total_ms / args.steps
+    # per-phase times: the same steps again, an event between the phases (which
+    # also keeps each kernel from being placed while the one before it drains,
+    # so every phase carries its launch; launch_floor_us is that cost alone)
+    for i in range(args.steps):
+        step(ev[i])
+    torch.cuda.synchronize(dev)
     phase_ms = {name: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in ev)
                 for j, name in enumerate(("layout", "dispatch", "combine"))}
     phase_med = {name: statistics.median(e[j].elapsed_time(e[j + 1]) for e in ev)
                  for j, name in enumerate(("layout", "dispatch", "combine"))}
+    floor_us = launch_floor_us(stream, dev, args.steps)
+    layout_alone = None if args.cached else layout_replay_us(ep, cfg, idx, lay, ws, stream, dev)
 
     # algorithmic bytes from this layout's counts
     ntpr = int(lay.num_tokens_per_rank.sum().item())
@@ -395,6 +403,8 @@ def native(args):
             k: {"us": phase_ms[k] * 1e3, "us_median": phase_med[k] * 1e3, "algorithmic_bytes": abytes[k],
                 "gbs": gbs[k], "frac_of_peak": gbs[k] / peak, "frac_of_nominal": gbs[k] / NOMINAL_HBM_GBS}
             for k in ("layout", "dispatch", "combine")},
+        "launch_floor_us": floor_us,
+        "layout_replay_us": layout_alone,
         "roofline": {"kernel": f"{dominant}_kernel", "bound": "hbm", "achieved": gbs[dominant],
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": gbs[dominant] / peak, "traffic": ncu_traffic(f"{dominant}_kernel", wl, R * T),
@@ -477,6 +487,39 @@ def graph_replay(ep, cfg, idx, lay, ws, x, sf, w, recv, y, out, stream, dev, arg
     ms = max_over_ranks(world, a.elapsed_time(b))
     return {"ms_per_step": ms / args.steps, "value": whole_job_rate(world, units, ms, args.steps),
             "unit": "tokens/s"}
+
+
+def launch_floor_us(stream, dev, steps):
+    """Event-bracketed time of an empty launch (a one-element tensor fill): the
+    fixed cost inside every per-phase figure."""
+    t = torch.zeros(1, device=dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in evs:
+        a.record(stream)
+        t.fill_(1.0)
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    return statistics.median(a.elapsed_time(b) for a, b in evs) * 1e3
+
+
+def layout_replay_us(ep, cfg, idx, lay, ws, stream, dev, n=20):
+    """The layout alone, n calls captured in one CUDA graph and replayed: its
+    time per call without host launches or events between calls."""
+    cs = torch.cuda.Stream(dev)
+    cs.wait_stream(stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cs), torch.cuda.graph(g, stream=cs):
+        for _ in range(n):
+            ep.ep_get_dispatch_layout(cfg, idx, lay, ws, cs)
+    g.replay()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(5):
+        g.replay()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    return a.elapsed_time(b) * 1e3 / (5 * n)
 
 
 def launches_per_step(wl, cached=False):

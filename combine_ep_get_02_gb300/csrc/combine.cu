@@ -23,6 +23,8 @@ __global__ void __launch_bounds__(kCopyThreads) combine_kernel(CombineArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
   const int nchunk = a.H >> 3;  // 8 bf16 per chunk
+  pdl_launch_dependents();
+  pdl_wait();
 
   // A work unit is one token's column range (a token is split into a.splits
   // ranges of a.split_chunks 16-byte chunks when tokens are too few to keep
@@ -149,8 +151,7 @@ cudaError_t launch_one(const CombineArgs& args, int num_sms, cudaStream_t stream
   const int64_t need = (a.num_tokens * a.splits + kWarps - 1) / kWarps;
   if (ctas > need) ctas = need;
   if (ctas < 1) return cudaSuccess;
-  kern<<<static_cast<unsigned>(ctas), kCopyThreads, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_chained(kern, dim3(static_cast<unsigned>(ctas)), dim3(kCopyThreads), 0, stream, a);
 }
 
 }  // namespace

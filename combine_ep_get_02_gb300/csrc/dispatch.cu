@@ -38,6 +38,8 @@ __global__ void __launch_bounds__(kCopyThreads, kKind == kCastRow ? 2 : 4) dispa
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t gwarp = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
   const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
+  pdl_launch_dependents();
+  pdl_wait();
 
   // tokens from the work queue; the next token's routing loads, and the one
   // after it is taken, while this token's row streams
@@ -149,8 +151,7 @@ cudaError_t launch_one(const DispatchArgs& a, int num_sms, cudaStream_t stream) 
   const int64_t need = ((a.zero_padding && a.E > a.num_tokens ? a.E : a.num_tokens) + kWarps - 1) / kWarps;
   if (ctas > need) ctas = need;
   if (ctas < 1) return cudaSuccess;
-  kern<<<static_cast<unsigned>(ctas), kCopyThreads, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_chained(kern, dim3(static_cast<unsigned>(ctas)), dim3(kCopyThreads), 0, stream, a);
 }
 
 }  // namespace

@@ -48,6 +48,8 @@ __global__ void __launch_bounds__(kBulkThreads) dispatch_bulk_kernel(DispatchArg
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncwarp();
+  pdl_launch_dependents();
+  pdl_wait();
 
   // pieces run (token, 0..pieces-1) for the warp's tokens (its fixed two, then
   // those it takes from the work queue) in turn; consecutive pieces alternate
@@ -141,7 +143,20 @@ int dispatch_bulk_stage_bytes(int row_bytes) {
 
 cudaError_t launch_dispatch_bulk(const Geometry& g, const DispatchArgs& a, int num_sms, cudaStream_t stream) {
   const int stage_bytes = dispatch_bulk_stage_bytes(a.in_row_bytes);
-  const size_t smem = static_cast<size_t>(kBulkWarps) * kBulkStages * stage_bytes;
+  size_t smem = static_cast<size_t>(kBulkWarps) * kBulkStages * stage_bytes;
+  // One CTA per SM, whatever the stage size: the grid is one CTA per SM, and
+  // the launch may be placed while the kernel before it drains (see pdl_wait),
+  // when SMs with free shared memory could otherwise take several CTAs each
+  // and leave others without. So ask for more than half an SM's shared memory.
+  static int sm_smem = 0;
+  if (sm_smem == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess)
+      return cudaErrorUnknown;
+  }
+  const size_t half = static_cast<size_t>(sm_smem) / 2 + 1024;
+  if (smem < half) smem = half;
   auto kern = g.expand ? dispatch_bulk_kernel<true> : dispatch_bulk_kernel<false>;
   int per_sm = resident_ctas(reinterpret_cast<const void*>(kern), kBulkThreads, smem);
   if (per_sm < 0) return cudaErrorUnknown;
@@ -152,8 +167,7 @@ cudaError_t launch_dispatch_bulk(const Geometry& g, const DispatchArgs& a, int n
   const int64_t need = (work + kBulkWarps - 1) / kBulkWarps;
   if (ctas > need) ctas = need;
   if (ctas < 1) return cudaSuccess;
-  kern<<<static_cast<unsigned>(ctas), kBulkThreads, smem, stream>>>(a, stage_bytes);
-  return cudaGetLastError();
+  return launch_chained(kern, dim3(static_cast<unsigned>(ctas)), dim3(kBulkThreads), smem, stream, a, stage_bytes);
 }
 
 }  // namespace ep

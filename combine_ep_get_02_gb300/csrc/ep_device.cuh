@@ -62,6 +62,17 @@ __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float a, float b) {
   return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
 }
 
+// ---- programmatic dependent launch ------------------------------------------
+// The library's kernels are launched with programmatic stream serialization:
+// a kernel may be placed on the SMs while the kernel before it on the stream
+// drains. Each kernel lets its successor be placed as soon as it starts, and
+// waits for its predecessor's completion (and memory) before it reads or
+// writes global memory: its inputs may be that kernel's outputs.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---- bulk copies (cp.async.bulk) and mbarriers -----------------------------
 
 constexpr uint32_t kBulkWaitLimit = 1u << 24;  // try_wait rounds before a wait gives up

@@ -188,6 +188,25 @@ cudaError_t launch_combine(const Geometry& g, const CombineArgs& a, int num_sms,
 
 int device_sm_count();
 
+// Launch `kernel` with programmatic stream serialization (see pdl_wait): it may
+// be placed on the SMs while the previous kernel on the stream drains; it waits
+// for that kernel before it touches global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_chained(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                           Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Resident CTAs per SM of `kernel` at `threads` threads and `smem` bytes of
 // dynamic shared memory on the current device, raising the kernel's dynamic
 // shared-memory limit first when smem needs it. Asked of the runtime once per

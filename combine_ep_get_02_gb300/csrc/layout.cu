@@ -205,11 +205,13 @@ __global__ void __launch_bounds__(THREADS) layout_kernel(LayoutArgs a) {
   const int t_begin = min(a.T, c * a.TB), t_end = min(a.T, t_begin + a.TB);
   const int64_t tok_base = static_cast<int64_t>(s) * a.T;
 
+  pdl_launch_dependents();
   for (int e = tid; e < E; e += THREADS) cnt_e[e] = 0;
   if (a.expand)
     for (int i = tid; i < WARPS * E; i += THREADS) ebits[i] = 0;
   if (tid < R) cnt_d[tid] = 0;
   __syncthreads();
+  pdl_wait();
 
   // ---- pass 1: this CTA's counts per destination and per expert
   bool bad = false;
@@ -420,8 +422,10 @@ __global__ void __launch_bounds__(kRowsThreads) layout_rows_kernel(LayoutArgs a)
   const int t_begin = min(a.T, c * a.TB), t_end = min(a.T, t_begin + a.TB);
   const int64_t tok_base = static_cast<int64_t>(s) * a.T;
 
+  pdl_launch_dependents();
   for (int e = tid; e < E; e += THREADS) cnt_e[e] = 0;
   __syncthreads();
+  pdl_wait();
 
   // ---- pass 1: every round's lanes at once, counted per expert and per
   // (round, warp, destination)
@@ -548,6 +552,8 @@ __global__ void __launch_bounds__(kRowsThreads) layout_rows_kernel(LayoutArgs a)
 __global__ void __launch_bounds__(kLayoutThreads) layout_expert_scan_kernel(LayoutArgs a) {
   constexpr int kCols = 32, kGroups = kLayoutThreads / kCols;
   __shared__ int32_t part[kGroups][kCols];
+  pdl_launch_dependents();
+  pdl_wait();
   const int ci = threadIdx.x % kCols, g = threadIdx.x / kCols;
   const int e = blockIdx.x * kCols + ci;
   const int R = a.R, E = a.E;
@@ -582,6 +588,8 @@ __global__ void __launch_bounds__(kLayoutThreads) layout_expand_kernel(LayoutArg
   int32_t* off = smem + a.E;        // [E]: this source's cross-source offsets
   __shared__ int32_t size_d[kMaxRanks];
   const int tid = threadIdx.x;
+  pdl_launch_dependents();
+  pdl_wait();
   const int s = blockIdx.x / a.C, c = blockIdx.x % a.C;
   const int E = a.E, L = a.L, R = a.R;
   for (int e = tid; e < E; e += kLayoutThreads) {
@@ -654,13 +662,15 @@ cudaError_t launch_clusters(Kernel kernel, const Geometry& g, const LayoutArgs& 
   cfg.blockDim = dim3(static_cast<unsigned>(threads));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = static_cast<unsigned>(a.C);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see pdl_wait
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
@@ -709,15 +719,17 @@ cudaError_t launch_layout(const Geometry& g, const LayoutArgs& args, int num_pro
     err = g.K <= 8 ? launch_main<8, 256>(g, a, stream) : launch_main<32, 256>(g, a, stream);
   if (err != cudaSuccess) return err;
   if (g.expand) {
-    layout_expert_scan_kernel<<<(g.E + 31) / 32, kLayoutThreads, 0, stream>>>(a);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if ((err = launch_chained(layout_expert_scan_kernel, dim3((g.E + 31) / 32), dim3(kLayoutThreads), 0, stream,
+                              a)) != cudaSuccess)
+      return err;
     const size_t smem2 = 2 * sizeof(int32_t) * g.E;
     if (smem2 > 32 * 1024 &&
         (err = cudaFuncSetAttribute(layout_expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(smem2))) != cudaSuccess)
       return err;
-    layout_expand_kernel<<<g.R * C, kLayoutThreads, smem2, stream>>>(a);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if ((err = launch_chained(layout_expand_kernel, dim3(g.R * C), dim3(kLayoutThreads), smem2, stream, a)) !=
+        cudaSuccess)
+      return err;
   }
   return cudaSuccess;
 }
