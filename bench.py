@@ -75,6 +75,8 @@ def parse():
                    help="only time one step's host<->device copies (the end-to-end bound), nothing else")
     p.add_argument("--no-ceiling", action="store_true",
                    help="skip the one-read, many-write reference copy timed at the dispatch's byte counts")
+    p.add_argument("--hbm-sweep", action="store_true",
+                   help="only measure HBM bandwidth against the read:write mix (fan-out copies, torch copy/fill)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline sample")
@@ -356,7 +358,7 @@ def native(args):
     phase_med = {name: statistics.median(e[j].elapsed_time(e[j + 1]) for e in ev)
                  for j, name in enumerate(("layout", "dispatch", "combine"))}
     floor_us = launch_floor_us(stream, dev, args.steps)
-    layout_alone = None if args.cached else layout_replay_us(ep, cfg, idx, lay, ws, stream, dev)
+    layout_alone = None if (args.cached or args.no_graph) else layout_replay_us(ep, cfg, idx, lay, ws, stream, dev)
 
     # algorithmic bytes from this layout's counts
     ntpr = int(lay.num_tokens_per_rank.sum().item())
@@ -368,6 +370,7 @@ def native(args):
     peak, peak_kind = peaks()
     gbs = {k: abytes[k] / (phase_ms[k] * 1e-3) / 1e9 for k in phase_ms}
     dominant = max(("dispatch", "combine"), key=lambda k: phase_ms[k])
+    dominant_kernel = "combine_kernel" if dominant == "combine" else dispatch_kernel_name(wl, args.copy_path)
 
     ceiling = None
     if not args.no_ceiling:
@@ -405,9 +408,9 @@ def native(args):
             for k in ("layout", "dispatch", "combine")},
         "launch_floor_us": floor_us,
         "layout_replay_us": layout_alone,
-        "roofline": {"kernel": f"{dominant}_kernel", "bound": "hbm", "achieved": gbs[dominant],
+        "roofline": {"kernel": dominant_kernel, "bound": "hbm", "achieved": gbs[dominant],
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": gbs[dominant] / peak, "traffic": ncu_traffic(f"{dominant}_kernel", wl, R * T),
+                     "frac": gbs[dominant] / peak, "traffic": ncu_traffic(dominant_kernel, wl, R * T),
                      "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": gbs[dominant] / NOMINAL_HBM_GBS},
         "clocks": clocks.summary(),
         "gpu_launches": args.steps * launches_per_step(wl, args.cached),
@@ -487,6 +490,16 @@ def graph_replay(ep, cfg, idx, lay, ws, x, sf, w, recv, y, out, stream, dev, arg
     ms = max_over_ranks(world, a.elapsed_time(b))
     return {"ms_per_step": ms / args.steps, "value": whole_job_rate(world, units, ms, args.steps),
             "unit": "tokens/s"}
+
+
+def dispatch_kernel_name(wl, copy_path):
+    """The dispatch kernel the library runs for this workload: the fused cast and
+    small or register-copy inputs take dispatch_kernel, unchanged rows of at
+    least 32 MiB (or copy path 2) the bulk-copy kernel."""
+    unchanged = not (wl.x_dtype == "bf16" and wl.recv_dtype == "fp8")
+    in_bytes = wl.num_ranks * wl.num_tokens * wl.hidden * (1 if wl.x_dtype == "fp8" else 2)
+    bulk = unchanged and (copy_path == 2 or (copy_path == 0 and in_bytes >= 32 << 20))
+    return "dispatch_bulk_kernel" if bulk else "dispatch_kernel"
 
 
 def launch_floor_us(stream, dev, steps):
@@ -823,6 +836,54 @@ def compare_sort(args):
                       "speedup": sum(old) / sum(det), "identical_after_sort": same}), flush=True)
 
 
+def hbm_sweep(args):
+    """Device-memory bandwidth against the read share of the traffic, with CUDA
+    events: the diagnostic fan-out copy (each row read once and written to a run
+    of fan consecutive rows, register and bulk methods) from mostly reads (1:64)
+    to mostly writes (64:1), beside torch's 1:1 copy and its fill (writes
+    only). About 4 GiB moved per point, rows of 14,336 bytes (a 7168-wide bf16
+    token)."""
+    import combine_ep_get_02_gb300 as ep
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    st = torch.cuda.current_stream(dev)
+
+    def timed(fn, reps=10):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        for _ in range(reps):
+            fn()
+        b.record(st)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) * 1e-3 / reps
+
+    gib = 1 << 30
+    buf = torch.empty(4 * gib, dtype=torch.uint8, device=dev)
+    out = {"mode": "hbm_sweep", "unit": "GB/s",
+           "torch_copy_1to1": 4 * gib / timed(lambda: buf[2 * gib:].copy_(buf[:2 * gib])) / 1e9,
+           "torch_fill_write_only": 4 * gib / timed(lambda: buf.view(torch.bfloat16).fill_(1.0)) / 1e9,
+           "fanout": []}
+    del buf
+    row = 14336
+    for num, den in ((1, 64), (1, 16), (1, 4), (1, 2), (1, 1), (2, 1), (3, 1), (3481, 1024), (4, 1), (8, 1),
+                     (16, 1), (64, 1)):
+        rows = int(4 * gib / row / (1 + num / den))
+        n_dst = rows * num // den
+        src = torch.empty(rows * row, dtype=torch.uint8, device=dev).random_()
+        dst = torch.empty(max(n_dst, 1) * row, dtype=torch.uint8, device=dev)
+        point = {"reads_per_write": f"{den}:{num}", "read_share": rows / (rows + n_dst)}
+        for method, name in ((0, "registers"), (1, "bulk")):
+            t = timed(lambda: ep.ep_diag_copy_fanout(src, dst, rows, row, num, den, 0, method, st))
+            point[name] = (rows + n_dst) * row / t / 1e9
+        out["fanout"].append(point)
+        del src, dst
+        torch.cuda.empty_cache()
+    print(json.dumps(out), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -831,6 +892,8 @@ def main():
         compare_sort(args)
     elif args.host_link:
         host_link(args)
+    elif args.hbm_sweep:
+        hbm_sweep(args)
     else:
         native(args)
 

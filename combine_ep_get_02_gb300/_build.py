@@ -41,7 +41,7 @@ def _deps():
 
 
 # translation unit that holds each kernel (and its launcher)
-KERNEL_UNITS = {"layout_kernel": "layout.cu", "dispatch_kernel": "dispatch.cu",
+KERNEL_UNITS = {"layout_kernel": "layout.cu", "layout_rows_kernel": "layout.cu", "dispatch_kernel": "dispatch.cu",
                 "dispatch_bulk_kernel": "dispatch_bulk.cu", "combine_kernel": "combine.cu"}
 
 

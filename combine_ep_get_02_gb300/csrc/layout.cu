@@ -120,10 +120,12 @@ __device__ __forceinline__ uint64_t load_token(const LayoutArgs& a, int64_t tok,
   return dmask;
 }
 
-// The end of every layout CTA: count it in; the last CTA of the grid turns the
-// receive counts (recv_cnt, published by each source's last CTA, fenced
-// before this) into their prefix sums over the row blocks and the first
-// packed row of each destination, then returns the counter to zero.
+// The end of every layout CTA, after the cluster barrier: count it in; the last
+// CTA of the grid turns the receive counts (recv_cnt, published and fenced by
+// each source's last CTA before that barrier) into their prefix sums over the
+// row blocks and the first packed row of each destination, then returns the
+// counter to zero. Only recv_cnt crosses CTAs here, so no other CTA fences
+// its own writes (the kernel's end publishes them).
 template <int THREADS>
 __device__ __forceinline__ void finish_receive_sums(const LayoutArgs& a, int32_t* s_cnt, int32_t* s_tot,
                                                     bool* s_last) {
@@ -265,6 +267,9 @@ __global__ void __launch_bounds__(THREADS) layout_kernel(LayoutArgs a) {
       const int total = base + cnt_d[d];
       a.num_tokens_per_rank[s * R + d] = total;
       a.recv_cnt[d * R + s] = total;
+      // visible before this CTA counts itself in (release: this fence, then the
+      // cluster barrier, then the arrival atomic); the last CTA reads recv_cnt
+      __threadfence();
     }
   }
   for (int e = tid; e < E; e += THREADS) {
@@ -389,7 +394,6 @@ __global__ void __launch_bounds__(THREADS) layout_kernel(LayoutArgs a) {
     }
   }
 
-  __threadfence();
   cluster.barrier_wait();
   finish_receive_sums<THREADS>(a, s_cnt, s_tot, &s_last);
 }
@@ -474,6 +478,9 @@ __global__ void __launch_bounds__(kRowsThreads) layout_rows_kernel(LayoutArgs a)
       const int total = base + cnt_d[d];
       a.num_tokens_per_rank[s * R + d] = total;
       a.recv_cnt[d * R + s] = total;
+      // visible before this CTA counts itself in (release: this fence, then the
+      // cluster barrier, then the arrival atomic); the last CTA reads recv_cnt
+      __threadfence();
     }
     int run = rb * a.M + base;
 #pragma unroll
@@ -541,7 +548,6 @@ __global__ void __launch_bounds__(kRowsThreads) layout_rows_kernel(LayoutArgs a)
     }
   }
 
-  __threadfence();
   cluster.barrier_wait();
   finish_receive_sums<THREADS>(a, s_cnt, s_tot, &s_last);
 }
