@@ -504,13 +504,18 @@ def dispatch_kernel_name(wl, copy_path):
 
 def launch_floor_us(stream, dev, steps):
     """Event-bracketed time of an empty launch (a one-element tensor fill): the
-    fixed cost inside every per-phase figure."""
+    fixed cost inside every per-phase figure. The GPU is first held busy
+    (torch.cuda._sleep) while all the launches are queued, so the figure is the
+    device's own gap, not the host's launch rate."""
     t = torch.zeros(1, device=dev)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-    for a, b in evs:
-        a.record(stream)
-        t.fill_(1.0)
-        b.record(stream)
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(5_000_000)  # a few ms of device time
+        for a, b in evs:
+            a.record(stream)
+            t.fill_(1.0)
+            b.record(stream)
     torch.cuda.synchronize(dev)
     return statistics.median(a.elapsed_time(b) for a, b in evs) * 1e3
 
