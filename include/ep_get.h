@@ -21,7 +21,11 @@
  *     workspace. The library never allocates, frees or synchronises, except
  *     ep_check_error, which synchronises the given stream.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream). All work
- *     is enqueued asynchronously on it, in call order.
+ *     is enqueued asynchronously on it, in call order. The layout, dispatch and
+ *     combine kernels are launched with programmatic stream serialization: one
+ *     may be placed on the SMs while the kernel before it drains, but it waits
+ *     for that kernel's completion before it reads or writes memory, so stream
+ *     order holds as for any launch.
  *   - Returns EP_OK (0) or a negative EP_ERR_* code. Host-detectable errors are
  *     reported before anything is enqueued. Errors found on the device (bad
  *     top-k values; a bounded wait that ran out; in the bounds-checked build
