@@ -672,7 +672,49 @@ def host_link(args):
     h2d = hx.numel() * hx.element_size() + hidx.numel() * 8 + hw.numel() * 4 + (0 if hsf is None else hsf.numel() * 4)
     print(json.dumps({"mode": "host_link", "workload": describe(wl), "h2d_bytes_per_step": h2d,
                       "d2h_bytes_per_step": hout.numel() * 2, "h2d_ms": f(True, False), "d2h_ms": f(False, True),
-                      "both_ms": f(True, True)}), flush=True)
+                      "both_ms": f(True, True), "zero_copy_gbs": zero_copy_rates(dev, st)}), flush=True)
+
+
+def zero_copy_rates(dev, st, nbytes=1 << 30):
+    """The same link driven by kernels instead of copy engines: the fan-out
+    diagnostic (1:1, register and bulk methods) reading pinned host memory into
+    device memory, writing device memory into pinned host memory, and both at
+    once on two streams."""
+    import combine_ep_get_02_gb300 as ep
+    row = 14336
+    rows = nbytes // row
+    h_in = torch.empty(rows * row, dtype=torch.uint8).pin_memory()
+    h_out = torch.empty(rows * row, dtype=torch.uint8).pin_memory()
+    d_in = torch.empty(rows * row, dtype=torch.uint8, device=dev)
+    d_out = torch.zeros(rows * row, dtype=torch.uint8, device=dev)
+    s0, s1 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def timed(fn, reps=5):
+        fn()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        for _ in range(reps):
+            fn()
+        b.record(st)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) * 1e-3 / reps
+
+    def both(method):
+        s0.wait_stream(st)
+        s1.wait_stream(st)
+        ep.ep_diag_copy_fanout(h_in, d_in, rows, row, 1, 1, 0, method, s0)
+        ep.ep_diag_copy_fanout(d_out, h_out, rows, row, 1, 1, 0, method, s1)
+        st.wait_stream(s0)
+        st.wait_stream(s1)
+
+    out = {}
+    for method, name in ((0, "registers"), (1, "bulk")):
+        out[name] = {
+            "read_host": rows * row / timed(lambda: ep.ep_diag_copy_fanout(h_in, d_in, rows, row, 1, 1, 0, method, st)) / 1e9,
+            "write_host": rows * row / timed(lambda: ep.ep_diag_copy_fanout(d_out, h_out, rows, row, 1, 1, 0, method, st)) / 1e9,
+            "both": 2 * rows * row / timed(lambda: both(method)) / 1e9}
+    return out
 
 
 def ncu_traffic(kernel, wl, n_tok):

@@ -122,16 +122,17 @@ __device__ __forceinline__ uint64_t load_token(const LayoutArgs& a, int64_t tok,
 
 // The end of every layout CTA, after the cluster barrier: count it in; the last
 // CTA of the grid turns the receive counts (recv_cnt, published and fenced by
-// each source's last CTA before that barrier) into their prefix sums over the
-// row blocks and the first packed row of each destination, then returns the
-// counter to zero. Only recv_cnt crosses CTAs here, so no other CTA fences
-// its own writes (the kernel's end publishes them).
+// each source's last CTA before it counts itself in) into their prefix sums
+// over the row blocks and the first packed row of each destination, then
+// returns the counter to zero. Only recv_cnt crosses CTAs here, so no other
+// CTA fences its own writes (the kernel's end publishes them).
 template <int THREADS>
 __device__ __forceinline__ void finish_receive_sums(const LayoutArgs& a, int32_t* s_cnt, int32_t* s_tot,
                                                     bool* s_last) {
   constexpr int WARPS = THREADS / 32;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int R = a.R;
+  __syncthreads();  // every fence of this CTA before its arrival
   if (tid == 0) *s_last = atomicAdd(a.done, 1u) == gridDim.x - 1u;
   __syncthreads();
   if (!*s_last) return;
@@ -267,9 +268,6 @@ __global__ void __launch_bounds__(THREADS) layout_kernel(LayoutArgs a) {
       const int total = base + cnt_d[d];
       a.num_tokens_per_rank[s * R + d] = total;
       a.recv_cnt[d * R + s] = total;
-      // visible before this CTA counts itself in (release: this fence, then the
-      // cluster barrier, then the arrival atomic); the last CTA reads recv_cnt
-      __threadfence();
     }
   }
   for (int e = tid; e < E; e += THREADS) {
@@ -394,6 +392,11 @@ __global__ void __launch_bounds__(THREADS) layout_kernel(LayoutArgs a) {
     }
   }
 
+  // the source's receive counts (written above by threads d < R of its last
+  // CTA) are visible before that CTA counts itself in: each writer fences here,
+  // at the end of its pass 2 so that the fence overlaps the other warps' work,
+  // and finish_receive_sums puts a barrier before the arrival atomic
+  if (c == a.C - 1 && tid < R) __threadfence();
   cluster.barrier_wait();
   finish_receive_sums<THREADS>(a, s_cnt, s_tot, &s_last);
 }
@@ -478,9 +481,6 @@ __global__ void __launch_bounds__(kRowsThreads) layout_rows_kernel(LayoutArgs a)
       const int total = base + cnt_d[d];
       a.num_tokens_per_rank[s * R + d] = total;
       a.recv_cnt[d * R + s] = total;
-      // visible before this CTA counts itself in (release: this fence, then the
-      // cluster barrier, then the arrival atomic); the last CTA reads recv_cnt
-      __threadfence();
     }
     int run = rb * a.M + base;
 #pragma unroll
@@ -548,6 +548,11 @@ __global__ void __launch_bounds__(kRowsThreads) layout_rows_kernel(LayoutArgs a)
     }
   }
 
+  // the source's receive counts (written above by threads d < R of its last
+  // CTA) are visible before that CTA counts itself in: each writer fences here,
+  // at the end of its pass 2 so that the fence overlaps the other warps' work,
+  // and finish_receive_sums puts a barrier before the arrival atomic
+  if (c == a.C - 1 && tid < R) __threadfence();
   cluster.barrier_wait();
   finish_receive_sums<THREADS>(a, s_cnt, s_tot, &s_last);
 }

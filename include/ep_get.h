@@ -322,10 +322,11 @@ int ep_diag_bf16_of_bits(uint32_t first, int64_t n, uint16_t* out, void* stream)
 /* Diagnostic copy for the bandwidth ceiling of a one-read, many-write stream
  * (no counterpart on the pages; the benchmark times it beside the dispatch,
  * whose scatter reads each token row once and writes it to each destination).
- * Row r of `src` (device, rows x row_bytes, 16-byte aligned) is read once and
+ * Row r of `src` (rows x row_bytes, 16-byte aligned) is read once and
  * written to rows floor(r*fan_num/fan_den) .. floor((r+1)*fan_num/fan_den) - 1
- * of `dst` (device, 16-byte aligned, floor(rows*fan_num/fan_den) rows of
- * row_bytes; the caller owns both). row_bytes: a positive multiple of 16;
+ * of `dst` (16-byte aligned, floor(rows*fan_num/fan_den) rows of row_bytes;
+ * the caller owns both). Either may be device memory or pinned host memory the
+ * device addresses directly (the benchmark times the host link that way). row_bytes: a positive multiple of 16;
  * 0 <= fan_num <= 2^20, fan_den >= 1, 0 <= rows <= 2^40; num_sms: SMs the grid
  * is sized for (0 = all). method 0: 16-byte register loads and stores; method
  * 1: bulk copies through shared memory (row_bytes <= 16384, else
