@@ -9,8 +9,9 @@
 // tokens; in the row form it takes them from a work queue in the workspace (a
 // token's cost grows with its number of destinations, so a static share would
 // leave the launch waiting on its heaviest warps).
-// Lanes 0..K-1 carry the token's top-k lanes and write the small sidecar rows
-// (routing of the lanes to that destination and the source metadata).
+// Lanes 0..K-1 carry the token's top-k lanes; the small sidecar rows (routing
+// of the lanes to each destination and the source metadata) are written by the
+// whole warp.
 // This register path carries the fused cast always, and rows that travel
 // unchanged when copy_path asks for it or the input is small; larger unchanged
 // inputs go to the bulk-copy kernel in dispatch_bulk.cu.
@@ -41,8 +42,9 @@ __global__ void __launch_bounds__(kCopyThreads, kKind == kCastRow ? 2 : 4) dispa
   pdl_launch_dependents();
   pdl_wait();
 
-  // tokens from the work queue; the next token's routing loads, and the one
-  // after it is taken, while this token's row streams
+  // the warp's tokens in turn (from the work queue in the row form): the next
+  // token's routing loads, and the one after it is taken, while this token's
+  // row streams
   UnitStream us = start_units(gwarp, nwarps, a.num_tokens, !kExpand);
   RawLane next = fetch_lane(a, us.cur, lane, kExpand, kAtomic);
   while (us.cur < a.num_tokens) {

@@ -51,9 +51,9 @@ __global__ void __launch_bounds__(kBulkThreads) dispatch_bulk_kernel(DispatchArg
   pdl_launch_dependents();
   pdl_wait();
 
-  // pieces run (token, 0..pieces-1) for the warp's tokens (its fixed two, then
-  // those it takes from the work queue) in turn; consecutive pieces alternate
-  // between the two stages.
+  // pieces run (token, 0..pieces-1) for the warp's tokens in turn (in the row
+  // form its fixed two, then those it takes from the work queue); consecutive
+  // pieces alternate between the two stages.
   // All lanes keep the same bookkeeping; lane 0 issues the copies.
   uint32_t parity = 0;   // bit s: parity of stage s's next completion
   uint32_t pending = 0;  // bit s: a load into stage s is in flight
