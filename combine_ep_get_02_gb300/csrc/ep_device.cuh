@@ -43,6 +43,32 @@ __device__ __forceinline__ void st16(void* p, const uint4& v) {
 // L2-coherent 32-bit load (bypasses L1): data another CTA wrote in this kernel.
 __device__ __forceinline__ int ld_cg(const int32_t* p) { return __ldcg(p); }
 
+// Start moving the line holding p into L2. Returns no value, so it may be
+// issued before the kernel waits for its predecessor (see pdl_wait): a line the
+// predecessor still writes is updated in L2, where the prefetch put it.
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// Cluster barrier halves without memory ordering: for "every CTA of the
+// cluster has started", which orders no data.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+
+// Atomic add at GPU scope with acquire-release semantics. Issued by one thread
+// between two CTA barriers, it publishes the writes the whole CTA made before
+// the first barrier and, when it returns, makes the writes published the same
+// way by the CTAs that added before it visible to the whole CTA after the
+// second (barriers order the CTA's threads; the release and acquire are
+// cumulative).
+__device__ __forceinline__ uint32_t atomic_add_acq_rel(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 // two bf16 (packed in a 32-bit word, low half first) -> two floats; exact
 __device__ __forceinline__ float2 bf16x2_to_f32x2(uint32_t w) {
   float2 r;

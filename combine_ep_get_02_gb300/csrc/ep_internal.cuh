@@ -100,8 +100,10 @@ struct LayoutArgs {
   int R, n_so, n_su, E, L, K, T, M, expand, align;
   int topk_vec;       // topk_idx rows can be read as 16-byte pairs
   uint32_t l_magic;   // e / L == __umulhi(e, l_magic) for e, L < 2^16
+  uint32_t so_magic;  // j / n_so == __umulhi(j, so_magic) for j, n_so < 2^16 (0: n_so == 1)
   int C;   // CTAs (one cluster) per source rank
   int TB;  // tokens per CTA
+  int EB;  // experts whose per-source totals each CTA of a cluster adds up (row-form kernel)
 };
 
 struct DispatchArgs {

@@ -17,6 +17,9 @@
 //   pass 2  warp prefix of the ballots plus the running base gives each lane's
 //           slot; the expanded layout ranks a lane among its expert's lanes with
 //           per-warp bitmaps of the tokens (source-local position).
+// layout_rows_kernel computes the same for the row form with top-k <= 8, with
+// every lane in registers and the counts pushed to the cluster peers instead of
+// read from them (its own comment below).
 // The last CTA of the grid to finish (a counter in the workspace, no waiting)
 // turns the receive counts into their prefix sums, and the destinations'
 // totals into the first packed row of each destination.
@@ -70,14 +73,13 @@ __device__ __forceinline__ int row_block(int s, int n_so, int n_su) {
   return n_so == 1 ? s : (s % n_su) * n_so + s / n_su;
 }
 
-// One token's top-k lanes in registers: expert per lane, -1 when masked or
-// invalid. Values outside [-1, E) are errors; in the expanded layout so is a
-// repeat of an earlier lane's expert. Returns the destination-rank mask.
+// One token's top-k entries as stored (int64), read with 16-byte loads when the
+// rows allow it; nothing is read for a token past the end.
 template <int KMAX>
-__device__ __forceinline__ uint64_t load_token(const LayoutArgs& a, int64_t tok, bool live, int (&e)[KMAX],
-                                               bool* bad) {
+__device__ __forceinline__ void load_lanes(const LayoutArgs& a, int64_t tok, bool live, int64_t (&v)[KMAX]) {
   const int64_t* p = a.topk_idx + tok * a.K;
-  int64_t v[KMAX];
+#pragma unroll
+  for (int k = 0; k < KMAX; ++k) v[k] = -1;
   if (live && a.topk_vec) {
 #pragma unroll
     for (int k = 0; k < KMAX; k += 2) {
@@ -92,6 +94,14 @@ __device__ __forceinline__ uint64_t load_token(const LayoutArgs& a, int64_t tok,
     for (int k = 0; k < KMAX; ++k)
       if (k < a.K) v[k] = __ldg(p + k);
   }
+}
+
+// One token's top-k lanes in registers: expert per lane, -1 when masked or
+// invalid. Values outside [-1, E) are errors; in the expanded layout so is a
+// repeat of an earlier lane's expert. Returns the destination-rank mask.
+template <int KMAX>
+__device__ __forceinline__ uint64_t decode_lanes(const LayoutArgs& a, const int64_t (&v)[KMAX], bool live,
+                                                 int (&e)[KMAX], bool* bad) {
   uint64_t dmask = 0;
 #pragma unroll
   for (int k = 0; k < KMAX; ++k) {
@@ -120,40 +130,66 @@ __device__ __forceinline__ uint64_t load_token(const LayoutArgs& a, int64_t tok,
   return dmask;
 }
 
-// The end of every layout CTA, after the cluster barrier: count it in; the last
-// CTA of the grid turns the receive counts (recv_cnt, published and fenced by
-// each source's last CTA before it counts itself in) into their prefix sums
-// over the row blocks and the first packed row of each destination, then
-// returns the counter to zero. Only recv_cnt crosses CTAs here, so no other
-// CTA fences its own writes (the kernel's end publishes them).
+template <int KMAX>
+__device__ __forceinline__ uint64_t load_token(const LayoutArgs& a, int64_t tok, bool live, int (&e)[KMAX],
+                                               bool* bad) {
+  int64_t v[KMAX];
+  load_lanes<KMAX>(a, tok, live, v);
+  return decode_lanes<KMAX>(a, v, live, e, bad);
+}
+
+// The end of every layout CTA: count it in; the last CTA of the grid turns the
+// receive counts (recv_cnt, written by each source's last CTA before it counts
+// itself in) into their prefix sums over the row blocks and the first packed
+// row of each destination, then returns the counter to zero. The count-in is
+// one acquire-release atomic between two CTA barriers: it publishes what the
+// CTA wrote and, for the last CTA, makes every other CTA's counts visible.
+// Only recv_cnt crosses CTAs here; the kernel's end publishes the rest.
 template <int THREADS>
-__device__ __forceinline__ void finish_receive_sums(const LayoutArgs& a, int32_t* s_cnt, int32_t* s_tot,
-                                                    bool* s_last) {
+__device__ __forceinline__ void finish_receive_sums(const LayoutArgs& a, int32_t* s_tot, bool* s_last) {
   constexpr int WARPS = THREADS / 32;
+  constexpr int kDests = (kMaxRanks + WARPS - 1) / WARPS, kChunks = (kMaxRanks + 31) / 32;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int R = a.R;
-  __syncthreads();  // every fence of this CTA before its arrival
-  if (tid == 0) *s_last = atomicAdd(a.done, 1u) == gridDim.x - 1u;
+  __syncthreads();
+  if (tid == 0) *s_last = atomic_add_acq_rel(a.done, 1u) == gridDim.x - 1u;
   __syncthreads();
   if (!*s_last) return;
-  __threadfence();
-  for (int i = tid; i < R * R; i += THREADS) s_cnt[i] = ld_cg(a.recv_cnt + i);
-  __syncthreads();
-  // one warp per destination: inclusive scan over the row blocks, 32 at a time
-  for (int d = warp; d < R; d += WARPS) {
+  // warp w scans destinations w, w + WARPS, ...: every count it needs is
+  // loaded first (row block j holds source src(j)), then one inclusive scan
+  // over the row blocks per destination, 32 at a time
+  int v[kDests][kChunks];
+#pragma unroll
+  for (int i = 0; i < kDests; ++i) {
+    const int d = warp + i * WARPS;
+#pragma unroll
+    for (int ch = 0; ch < kChunks; ++ch) {
+      const int j = ch * 32 + lane;
+      v[i][ch] = 0;
+      if (d < R && j < R) {
+        const int q = a.so_magic == 0 ? 0 : static_cast<int>(__umulhi(static_cast<uint32_t>(j), a.so_magic));
+        const int src = a.n_so == 1 ? j : (j - q * a.n_so) * a.n_su + q;
+        v[i][ch] = ld_cg(a.recv_cnt + d * R + src);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < kDests; ++i) {
+    const int d = warp + i * WARPS;
+    if (d >= R) break;
     int carry = 0;
-    for (int i0 = 0; i0 < R; i0 += 32) {
-      const int i = i0 + lane;  // row block i holds source src(i)
-      int v = 0;
-      if (i < R) v = s_cnt[d * R + (a.n_so == 1 ? i : (i % a.n_so) * a.n_su + i / a.n_so)];
+#pragma unroll
+    for (int ch = 0; ch < kChunks; ++ch) {
+      const int j = ch * 32 + lane;
+      int x = v[i][ch];
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const int u = __shfl_up_sync(kFullMask, v, o);
-        if (lane >= o) v += u;
+        const int u = __shfl_up_sync(kFullMask, x, o);
+        if (lane >= o) x += u;
       }
-      v += carry;
-      if (i < R) a.recv_psum[d * R + i] = v;
-      carry = __shfl_sync(kFullMask, v, 31);
+      x += carry;
+      if (j < R) a.recv_psum[d * R + j] = x;
+      carry = __shfl_sync(kFullMask, x, 31);
     }
     if (lane == 0) s_tot[d] = carry;
   }
@@ -166,14 +202,14 @@ __device__ __forceinline__ void finish_receive_sums(const LayoutArgs& a, int32_t
       for (int d0 = 0; d0 < R; d0 += 32) {
         const int d = d0 + lane;
         const int n = d < R ? s_tot[d] : 0;
-        int v = n;
+        int x = n;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-          const int u = __shfl_up_sync(kFullMask, v, o);
-          if (lane >= o) v += u;
+          const int u = __shfl_up_sync(kFullMask, x, o);
+          if (lane >= o) x += u;
         }
-        if (d < R) a.recv_region[d] = carry + v - n;
-        carry += __shfl_sync(kFullMask, v, 31);
+        if (d < R) a.recv_region[d] = carry + x - n;
+        carry += __shfl_sync(kFullMask, x, 31);
       }
       if (lane == 0) a.recv_region[R] = carry;
     }
@@ -196,7 +232,6 @@ __global__ void __launch_bounds__(THREADS) layout_kernel(LayoutArgs a) {
   __shared__ int32_t run_d[kMaxRanks];
   __shared__ uint32_t bal[WARPS][kMaxRanks];
   __shared__ int32_t wbase[WARPS][kMaxRanks];
-  __shared__ int32_t s_cnt[kMaxRanks * kMaxRanks];
   __shared__ int32_t s_tot[kMaxRanks];
   __shared__ bool s_last;
 
@@ -392,44 +427,56 @@ __global__ void __launch_bounds__(THREADS) layout_kernel(LayoutArgs a) {
     }
   }
 
-  // the source's receive counts (written above by threads d < R of its last
-  // CTA) are visible before that CTA counts itself in: each writer fences here,
-  // at the end of its pass 2 so that the fence overlaps the other warps' work,
-  // and finish_receive_sums puts a barrier before the arrival atomic
-  if (c == a.C - 1 && tid < R) __threadfence();
   cluster.barrier_wait();
-  finish_receive_sums<THREADS>(a, s_cnt, s_tot, &s_last);
+  finish_receive_sums<THREADS>(a, s_tot, &s_last);
 }
 
-// Row form (no expanded positions) with top-k <= 8: the same counts, scan and
-// slots as layout_kernel, reorganised for latency. Each CTA (256 threads) holds
-// every round of its tokens' lanes in registers and, in pass 1, records each
-// (round, warp)'s token count per destination; after the cluster scan one
-// barrier turns those counts into every (round, warp)'s base, so pass 2 runs
-// without barriers: a lane's rank among its warp's tokens to destination d is
-// the popcount below it of column d of the warp's destination bit matrix
-// (fetched from lane d with a shuffle).
+// Row form (no expanded positions) with top-k <= 8: the same counts and slots
+// as layout_kernel, reorganised for latency.
+//  - Each CTA (256 threads) holds every round of its tokens' lanes in
+//    registers; all routing rows are requested at once (and prefetched to L2
+//    before the wait for the previous kernel).
+//  - Pass 1 records each (round, warp)'s token count per destination. The CTA
+//    then pushes its counts into its cluster peers' shared memory: its
+//    destination counts to every later CTA of the source, and its count of each
+//    expert to the CTA that totals that expert. After one cluster barrier every
+//    sum a CTA needs is in its own shared memory.
+//  - One CTA barrier turns the (round, warp) counts into bases, so pass 2 runs
+//    without barriers: a lane's rank among its warp's tokens to destination d
+//    is the popcount below it of column d of the warp's destination bit matrix
+//    (fetched from lane d with a shuffle).
+// No CTA reads another's shared memory after the barrier, so none waits for its
+// peers before it exits.
 template <int ROUNDS>
-__global__ void __launch_bounds__(kRowsThreads) layout_rows_kernel(LayoutArgs a) {
+__global__ void __launch_bounds__(kRowsThreads, 1) layout_rows_kernel(LayoutArgs a) {
   constexpr int THREADS = kRowsThreads, WARPS = THREADS / 32, KMAX = 8;
+  constexpr int RW = ROUNDS * WARPS;  // (round, warp) pairs
   cg::cluster_group cluster = cg::this_cluster();
   extern __shared__ int32_t smem[];
-  int32_t* cnt_e = smem;  // [E]
-  __shared__ int32_t cnt_d[kMaxRanks];
-  __shared__ int32_t wcnt[ROUNDS * WARPS][kMaxRanks];  // counts of each (round, warp), then their bases
-  __shared__ int32_t s_cnt[kMaxRanks * kMaxRanks];
+  int32_t* cnt_e = smem;          // [E]: this CTA's lanes per expert
+  int32_t* in_e = smem + a.E;     // [C][EB]: every peer's count of the experts this CTA totals
+  __shared__ int32_t in_d[8][kMaxRanks];  // [q][d]: CTA q's tokens to d (q < this CTA; own at q == c)
+  __shared__ int32_t wcnt[RW][kMaxRanks];  // counts of each (round, warp), then their bases
   __shared__ int32_t s_tot[kMaxRanks];
   __shared__ bool s_last;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const unsigned lt = lanemask_lt();
-  const int R = a.R, E = a.E;
-  const int s = blockIdx.x / a.C;
+  const int R = a.R, E = a.E, C = a.C, EB = a.EB;
+  const int s = blockIdx.x / C;
   const int c = static_cast<int>(cluster.block_rank());
   const int t_begin = min(a.T, c * a.TB), t_end = min(a.T, t_begin + a.TB);
   const int64_t tok_base = static_cast<int64_t>(s) * a.T;
 
   pdl_launch_dependents();
+#pragma unroll
+  for (int r = 0; r < ROUNDS; ++r) {
+    const int t = t_begin + r * THREADS + tid;
+    if (t < t_end) prefetch_l2(a.topk_idx + (tok_base + t) * a.K);
+  }
+  // every CTA of the cluster has started before any writes to a peer's shared
+  // memory (the matching wait comes after pass 1)
+  cluster_arrive_relaxed();
   for (int e = tid; e < E; e += THREADS) cnt_e[e] = 0;
   __syncthreads();
   pdl_wait();
@@ -440,10 +487,18 @@ __global__ void __launch_bounds__(kRowsThreads) layout_rows_kernel(LayoutArgs a)
   int e[ROUNDS][KMAX];
   uint64_t dmask[ROUNDS];
   uint32_t col_lo[ROUNDS], col_hi[ROUNDS];
+  {
+    int64_t v[ROUNDS][KMAX];
 #pragma unroll
-  for (int r = 0; r < ROUNDS; ++r) {
-    const int t = t_begin + r * THREADS + tid;
-    dmask[r] = load_token<KMAX>(a, tok_base + t, t < t_end, e[r], &bad);
+    for (int r = 0; r < ROUNDS; ++r) {
+      const int t = t_begin + r * THREADS + tid;
+      load_lanes<KMAX>(a, tok_base + t, t < t_end, v[r]);
+    }
+#pragma unroll
+    for (int r = 0; r < ROUNDS; ++r) {
+      const int t = t_begin + r * THREADS + tid;
+      dmask[r] = decode_lanes<KMAX>(a, v[r], t < t_end, e[r], &bad);
+    }
   }
 #pragma unroll
   for (int r = 0; r < ROUNDS; ++r) {
@@ -461,45 +516,56 @@ __global__ void __launch_bounds__(kRowsThreads) layout_rows_kernel(LayoutArgs a)
   }
   if (bad) atomicOr(a.err, kErrBadTopk);
   __syncthreads();
+
+  // ---- push the counts to the peers, then one cluster barrier
+  cluster_wait();
   for (int d = tid; d < R; d += THREADS) {
     int n = 0;
 #pragma unroll
-    for (int rw = 0; rw < ROUNDS * WARPS; ++rw) n += wcnt[rw][d];
-    cnt_d[d] = n;
+    for (int rw = 0; rw < RW; ++rw) n += wcnt[rw][d];
+    in_d[c][d] = n;
+    for (int q = c + 1; q < C; ++q) cluster.map_shared_rank(&in_d[0][0], q)[c * kMaxRanks + d] = n;
+  }
+  for (int q = 0; q < C; ++q) {
+    int32_t* dst = (q == c ? in_e : cluster.map_shared_rank(in_e, q)) + c * EB;
+    for (int j = tid; j < EB; j += THREADS) {
+      const int x = q * EB + j;
+      if (x < E) dst[j] = cnt_e[x];
+    }
   }
   cluster.sync();
 
-  // ---- scan across the cluster: counts of the CTAs before this one; this
-  // CTA's (round, warp) counts become their bases
+  // ---- bases: this CTA's (round, warp) counts become their first slots
   const int rb = row_block(s, a.n_so, a.n_su);
   for (int d = tid; d < R; d += THREADS) {
     int base = 0;
 #pragma unroll
     for (int q = 0; q < 8; ++q)
-      if (q < c) base += cluster.map_shared_rank(cnt_d, q)[d];
-    if (c == a.C - 1) {  // the source's totals
-      const int total = base + cnt_d[d];
+      if (q < c) base += in_d[q][d];
+    if (c == C - 1) {  // the source's totals
+      const int total = base + in_d[c][d];
       a.num_tokens_per_rank[s * R + d] = total;
       a.recv_cnt[d * R + s] = total;
     }
     int run = rb * a.M + base;
 #pragma unroll
-    for (int rw = 0; rw < ROUNDS * WARPS; ++rw) {
+    for (int rw = 0; rw < RW; ++rw) {
       const int n = wcnt[rw][d];
       wcnt[rw][d] = run;
       run += n;
     }
   }
-  for (int x = tid; x < E; x += THREADS) {
-    int base = 0;
+  // this CTA's share of the source's per-expert totals
+  for (int j = tid; j < EB; j += THREADS) {
+    const int x = c * EB + j;
+    if (x < E) {
+      int n = 0;
 #pragma unroll
-    for (int q = 0; q < 8; ++q)
-      if (q < c) base += cluster.map_shared_rank(cnt_e, q)[x];
-    if (c == a.C - 1) a.num_tokens_per_expert[s * E + x] = base + cnt_e[x];
+      for (int q = 0; q < 8; ++q)
+        if (q < C) n += in_e[q * EB + j];
+      a.num_tokens_per_expert[s * E + x] = n;
+    }
   }
-  // other CTAs may still read this CTA's counts: they are left untouched, and
-  // the CTA waits for the whole cluster before it exits
-  cluster.barrier_arrive();
   __syncthreads();
 
   // ---- pass 2: slots, no barriers
@@ -534,13 +600,20 @@ __global__ void __launch_bounds__(kRowsThreads) layout_rows_kernel(LayoutArgs a)
           if (k < a.K) srow[k] = slot[k];
       }
       uint8_t* row = a.is_token_in_rank + tok * R;
-      if ((R & 3) == 0) {
+      if ((R & 15) == 0 && aligned16(row)) {
+        for (int d = 0; d < R; d += 16) {
+          uint32_t w[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t m = static_cast<uint32_t>(dmask[r] >> (d + 4 * i)) & 15u;
+            w[i] = (m & 1u) | (m & 2u) << 7 | (m & 4u) << 14 | (m & 8u) << 21;
+          }
+          *reinterpret_cast<uint4*>(row + d) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      } else if ((R & 3) == 0) {
         for (int d = 0; d < R; d += 4) {
-          const uint32_t v = static_cast<uint32_t>((dmask[r] >> d) & 1) |
-                             static_cast<uint32_t>((dmask[r] >> (d + 1)) & 1) << 8 |
-                             static_cast<uint32_t>((dmask[r] >> (d + 2)) & 1) << 16 |
-                             static_cast<uint32_t>((dmask[r] >> (d + 3)) & 1) << 24;
-          *reinterpret_cast<uint32_t*>(row + d) = v;
+          const uint32_t m = static_cast<uint32_t>(dmask[r] >> d) & 15u;
+          *reinterpret_cast<uint32_t*>(row + d) = (m & 1u) | (m & 2u) << 7 | (m & 4u) << 14 | (m & 8u) << 21;
         }
       } else {
         for (int d = 0; d < R; ++d) row[d] = static_cast<uint8_t>((dmask[r] >> d) & 1);
@@ -548,13 +621,7 @@ __global__ void __launch_bounds__(kRowsThreads) layout_rows_kernel(LayoutArgs a)
     }
   }
 
-  // the source's receive counts (written above by threads d < R of its last
-  // CTA) are visible before that CTA counts itself in: each writer fences here,
-  // at the end of its pass 2 so that the fence overlaps the other warps' work,
-  // and finish_receive_sums puts a barrier before the arrival atomic
-  if (c == a.C - 1 && tid < R) __threadfence();
-  cluster.barrier_wait();
-  finish_receive_sums<THREADS>(a, s_cnt, s_tot, &s_last);
+  finish_receive_sums<THREADS>(a, s_tot, &s_last);
 }
 
 // Expanded layout, step 2: for 32 experts per CTA, the exclusive prefix of the
@@ -719,8 +786,10 @@ cudaError_t launch_layout(const Geometry& g, const LayoutArgs& args, int num_pro
   a.C = C;
   a.TB = (g.T + C - 1) / C;
   a.l_magic = g.L == 1 ? 0u : static_cast<uint32_t>((0x100000000ull + g.L - 1) / g.L);
+  a.so_magic = g.n_so == 1 ? 0u : static_cast<uint32_t>((0x100000000ull + g.n_so - 1) / g.n_so);
+  a.EB = (g.E + C - 1) / C;
   const int rounds = (a.TB + threads - 1) / threads;
-  const size_t smem_rows = sizeof(int32_t) * g.E;
+  const size_t smem_rows = sizeof(int32_t) * (g.E + static_cast<size_t>(C) * a.EB);
   cudaError_t err;
   if (rows && rounds <= 1)
     err = launch_clusters(layout_rows_kernel<1>, g, a, threads, smem_rows, stream);
