@@ -57,16 +57,23 @@ __device__ __forceinline__ void cluster_arrive_relaxed() {
 }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
 
-// Atomic add at GPU scope with acquire-release semantics. Issued by one thread
-// between two CTA barriers, it publishes the writes the whole CTA made before
-// the first barrier and, when it returns, makes the writes published the same
-// way by the CTAs that added before it visible to the whole CTA after the
-// second (barriers order the CTA's threads; the release and acquire are
-// cumulative).
-__device__ __forceinline__ uint32_t atomic_add_acq_rel(uint32_t* p, uint32_t v) {
+// Atomic add at GPU scope with release semantics. Issued by one thread after a
+// CTA barrier, it publishes the writes the whole CTA made before the barrier
+// (the barrier orders the CTA's threads; the release is cumulative). It orders
+// nothing after it, so the thread goes on without waiting for the result.
+__device__ __forceinline__ uint32_t atomic_add_release(uint32_t* p, uint32_t v) {
   uint32_t old;
-  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  asm volatile("atom.release.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
   return old;
+}
+
+// Load at GPU scope with acquire semantics. Reading a counter that release
+// atomics (above) incremented, it makes what each of them published visible
+// to this thread's later accesses and, past a CTA barrier, to the whole CTA's.
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
 }
 
 // two bf16 (packed in a 32-bit word, low half first) -> two floats; exact

@@ -138,21 +138,29 @@ __device__ __forceinline__ uint64_t load_token(const LayoutArgs& a, int64_t tok,
   return decode_lanes<KMAX>(a, v, live, e, bad);
 }
 
-// The end of every layout CTA: count it in; the last CTA of the grid turns the
-// receive counts (recv_cnt, written by each source's last CTA before it counts
-// itself in) into their prefix sums over the row blocks and the first packed
-// row of each destination, then returns the counter to zero. The count-in is
-// one acquire-release atomic between two CTA barriers: it publishes what the
-// CTA wrote and, for the last CTA, makes every other CTA's counts visible.
-// Only recv_cnt crosses CTAs here; the kernel's end publishes the rest.
+// Count this CTA in: called by one thread after a CTA barrier that follows the
+// CTA's writes of the receive counts (recv_cnt, by each source's last CTA). A
+// release atomic: it publishes those writes without waiting for its result;
+// the result says at the CTA's end whether it was the last to count in.
+__device__ __forceinline__ uint32_t count_in(const LayoutArgs& a) { return atomic_add_release(a.done, 1u); }
+
+// The end of every layout CTA: the last CTA to count in (thread 0 holds the
+// counter's old value) reads the counter once more with acquire semantics,
+// which makes every other CTA's published receive counts visible, turns them
+// into their prefix sums over the row blocks and the first packed row of each
+// destination, then returns the counter to zero.
 template <int THREADS>
-__device__ __forceinline__ void finish_receive_sums(const LayoutArgs& a, int32_t* s_tot, bool* s_last) {
+__device__ __forceinline__ void finish_receive_sums(const LayoutArgs& a, uint32_t old, int32_t* s_tot,
+                                                    bool* s_last) {
   constexpr int WARPS = THREADS / 32;
   constexpr int kDests = (kMaxRanks + WARPS - 1) / WARPS, kChunks = (kMaxRanks + 31) / 32;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int R = a.R;
-  __syncthreads();
-  if (tid == 0) *s_last = atomic_add_acq_rel(a.done, 1u) == gridDim.x - 1u;
+  if (tid == 0) {
+    const bool last = old == gridDim.x - 1u;
+    if (last) ld_acquire(a.done);
+    *s_last = last;
+  }
   __syncthreads();
   if (!*s_last) return;
   // warp w scans destinations w, w + WARPS, ...: every count it needs is
@@ -317,6 +325,8 @@ __global__ void __launch_bounds__(THREADS) layout_kernel(LayoutArgs a) {
   // the CTA waits for the whole cluster before it exits
   cluster.barrier_arrive();
   __syncthreads();
+  uint32_t arrived = 0;
+  if (tid == 0) arrived = count_in(a);
 
   // ---- pass 2: slots (and source-local expanded positions)
   {
@@ -428,7 +438,7 @@ __global__ void __launch_bounds__(THREADS) layout_kernel(LayoutArgs a) {
   }
 
   cluster.barrier_wait();
-  finish_receive_sums<THREADS>(a, s_tot, &s_last);
+  finish_receive_sums<THREADS>(a, arrived, s_tot, &s_last);
 }
 
 // Row form (no expanded positions) with top-k <= 8: the same counts and slots
@@ -444,7 +454,8 @@ __global__ void __launch_bounds__(THREADS) layout_kernel(LayoutArgs a) {
 //  - One CTA barrier turns the (round, warp) counts into bases, so pass 2 runs
 //    without barriers: a lane's rank among its warp's tokens to destination d
 //    is the popcount below it of column d of the warp's destination bit matrix
-//    (fetched from lane d with a shuffle).
+//    (fetched from lane d with a shuffle). The CTA counts itself in before
+//    pass 2 (see count_in).
 // No CTA reads another's shared memory after the barrier, so none waits for its
 // peers before it exits.
 template <int ROUNDS>
@@ -567,6 +578,8 @@ __global__ void __launch_bounds__(kRowsThreads, 1) layout_rows_kernel(LayoutArgs
     }
   }
   __syncthreads();
+  uint32_t arrived = 0;
+  if (tid == 0) arrived = count_in(a);
 
   // ---- pass 2: slots, no barriers
 #pragma unroll
@@ -621,7 +634,7 @@ __global__ void __launch_bounds__(kRowsThreads, 1) layout_rows_kernel(LayoutArgs
     }
   }
 
-  finish_receive_sums<THREADS>(a, s_tot, &s_last);
+  finish_receive_sums<THREADS>(a, arrived, s_tot, &s_last);
 }
 
 // Expanded layout, step 2: for 32 experts per CTA, the exclusive prefix of the
