@@ -358,7 +358,13 @@ def native(args):
     phase_med = {name: statistics.median(e[j].elapsed_time(e[j + 1]) for e in ev)
                  for j, name in enumerate(("layout", "dispatch", "combine"))}
     floor_us = launch_floor_us(stream, dev, args.steps)
-    layout_alone = None if (args.cached or args.no_graph) else layout_replay_us(ep, cfg, idx, lay, ws, stream, dev)
+    # each phase alone, replayed from a CUDA graph (no event or host launch between calls)
+    replay = {}
+    if not args.no_graph:
+        if not args.cached:
+            replay["layout"] = replay_us(lambda s: ep.ep_get_dispatch_layout(cfg, idx, lay, ws, s), stream, dev, 20)
+        replay["dispatch"] = replay_us(lambda s: ep.ep_dispatch(cfg, lay, x, sf, idx, w, recv, ws, s), stream, dev, 10)
+        replay["combine"] = replay_us(lambda s: ep.ep_combine(cfg, lay, y, idx, w, out, ws, s), stream, dev, 10)
 
     # algorithmic bytes from this layout's counts
     ntpr = int(lay.num_tokens_per_rank.sum().item())
@@ -407,7 +413,9 @@ def native(args):
                 "gbs": gbs[k], "frac_of_peak": gbs[k] / peak, "frac_of_nominal": gbs[k] / NOMINAL_HBM_GBS}
             for k in ("layout", "dispatch", "combine")},
         "launch_floor_us": floor_us,
-        "layout_replay_us": layout_alone,
+        "layout_replay_us": replay.get("layout"),
+        "phase_replay": {k: {"us": v, "gbs": abytes[k] / (v * 1e-6) / 1e9, "frac_of_peak": abytes[k] / (v * 1e-6) / 1e9 / peak}
+                         for k, v in replay.items()},
         "roofline": {"kernel": dominant_kernel, "bound": "hbm", "achieved": gbs[dominant],
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": gbs[dominant] / peak, "traffic": ncu_traffic(dominant_kernel, wl, R * T),
@@ -520,15 +528,15 @@ def launch_floor_us(stream, dev, steps):
     return statistics.median(a.elapsed_time(b) for a, b in evs) * 1e3
 
 
-def layout_replay_us(ep, cfg, idx, lay, ws, stream, dev, n=20):
-    """The layout alone, n calls captured in one CUDA graph and replayed: its
-    time per call without host launches or events between calls."""
+def replay_us(fn, stream, dev, n):
+    """n calls of fn(stream) captured in one CUDA graph and replayed: the time per
+    call without host launches or events between calls."""
     cs = torch.cuda.Stream(dev)
     cs.wait_stream(stream)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(cs), torch.cuda.graph(g, stream=cs):
         for _ in range(n):
-            ep.ep_get_dispatch_layout(cfg, idx, lay, ws, cs)
+            fn(cs)
     g.replay()
     torch.cuda.synchronize(dev)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
