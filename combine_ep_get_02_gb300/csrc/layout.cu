@@ -441,31 +441,41 @@ __global__ void __launch_bounds__(THREADS) layout_kernel(LayoutArgs a) {
   finish_receive_sums<THREADS>(a, arrived, s_tot, &s_last);
 }
 
-// Row form (no expanded positions) with top-k <= 8: the same counts and slots
-// as layout_kernel, reorganised for latency.
+// Top-k <= 8, row form or expanded: the same counts, slots and source-local
+// expanded positions as layout_kernel, reorganised for latency.
 //  - Each CTA (256 threads) holds every round of its tokens' lanes in
 //    registers; all routing rows are requested at once (and prefetched to L2
 //    before the wait for the previous kernel).
-//  - Pass 1 records each (round, warp)'s token count per destination. The CTA
-//    then pushes its counts into its cluster peers' shared memory: its
-//    destination counts to every later CTA of the source, and its count of each
-//    expert to the CTA that totals that expert. After one cluster barrier every
-//    sum a CTA needs is in its own shared memory.
+//  - Pass 1 records each (round, warp)'s token count per destination and,
+//    expanded, a bitmap per (round, warp, expert) of the warp's tokens with a
+//    lane on that expert. The CTA then pushes its counts into its cluster
+//    peers' shared memory: its destination counts to every later CTA of the
+//    source, and its per-expert counts to the CTA that totals that expert (row
+//    form) or to every later CTA (expanded, whose positions need the prefix).
+//    After one cluster barrier every sum a CTA needs is in its own shared
+//    memory.
 //  - One CTA barrier turns the (round, warp) counts into bases, so pass 2 runs
 //    without barriers: a lane's rank among its warp's tokens to destination d
 //    is the popcount below it of column d of the warp's destination bit matrix
-//    (fetched from lane d with a shuffle). The CTA counts itself in before
-//    pass 2 (see count_in).
+//    (fetched from lane d with a shuffle); its rank among the lanes on expert e
+//    is the popcount below it of the warp's bitmap for e. The CTA counts itself
+//    in before pass 2 (see count_in).
 // No CTA reads another's shared memory after the barrier, so none waits for its
 // peers before it exits.
-template <int ROUNDS>
+//
+// dynamic shared memory: cnt_e [E] | row form: in_e [C][EB]; expanded: in_e
+// [C][E], ebits [RW][E], ebase [RW][E]
+template <int ROUNDS, bool EXPAND>
 __global__ void __launch_bounds__(kRowsThreads, 1) layout_rows_kernel(LayoutArgs a) {
   constexpr int THREADS = kRowsThreads, WARPS = THREADS / 32, KMAX = 8;
   constexpr int RW = ROUNDS * WARPS;  // (round, warp) pairs
   cg::cluster_group cluster = cg::this_cluster();
+  const int R = a.R, E = a.E, C = a.C, EB = a.EB;
   extern __shared__ int32_t smem[];
-  int32_t* cnt_e = smem;          // [E]: this CTA's lanes per expert
-  int32_t* in_e = smem + a.E;     // [C][EB]: every peer's count of the experts this CTA totals
+  int32_t* cnt_e = smem;                                  // this CTA's lanes per expert
+  int32_t* in_e = smem + E;                               // peers' per-expert counts
+  uint32_t* ebits = reinterpret_cast<uint32_t*>(in_e + C * E);  // expanded only
+  int32_t* ebase = in_e + C * E + RW * E;                 // expanded only
   __shared__ int32_t in_d[8][kMaxRanks];  // [q][d]: CTA q's tokens to d (q < this CTA; own at q == c)
   __shared__ int32_t wcnt[RW][kMaxRanks];  // counts of each (round, warp), then their bases
   __shared__ int32_t s_tot[kMaxRanks];
@@ -473,7 +483,6 @@ __global__ void __launch_bounds__(kRowsThreads, 1) layout_rows_kernel(LayoutArgs
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const unsigned lt = lanemask_lt();
-  const int R = a.R, E = a.E, C = a.C, EB = a.EB;
   const int s = blockIdx.x / C;
   const int c = static_cast<int>(cluster.block_rank());
   const int t_begin = min(a.T, c * a.TB), t_end = min(a.T, t_begin + a.TB);
@@ -488,12 +497,16 @@ __global__ void __launch_bounds__(kRowsThreads, 1) layout_rows_kernel(LayoutArgs
   // every CTA of the cluster has started before any writes to a peer's shared
   // memory (the matching wait comes after pass 1)
   cluster_arrive_relaxed();
-  for (int e = tid; e < E; e += THREADS) cnt_e[e] = 0;
+  if constexpr (EXPAND) {
+    for (int i = tid; i < RW * E; i += THREADS) ebits[i] = 0u;
+  } else {
+    for (int e = tid; e < E; e += THREADS) cnt_e[e] = 0;
+  }
   __syncthreads();
   pdl_wait();
 
-  // ---- pass 1: every round's lanes at once, counted per expert and per
-  // (round, warp, destination)
+  // ---- pass 1: every round's lanes at once, counted per (round, warp,
+  // destination) and per expert (expanded: as per-(round, warp) bitmaps)
   bool bad = false;
   int e[ROUNDS][KMAX];
   uint64_t dmask[ROUNDS];
@@ -514,8 +527,12 @@ __global__ void __launch_bounds__(kRowsThreads, 1) layout_rows_kernel(LayoutArgs
 #pragma unroll
   for (int r = 0; r < ROUNDS; ++r) {
 #pragma unroll
-    for (int k = 0; k < KMAX; ++k)
-      if (e[r][k] >= 0) atomicAdd(&cnt_e[e[r][k]], 1);
+    for (int k = 0; k < KMAX; ++k) {
+      if (e[r][k] >= 0) {
+        if constexpr (EXPAND) atomicOr(&ebits[(r * WARPS + warp) * E + e[r][k]], 1u << lane);
+        else atomicAdd(&cnt_e[e[r][k]], 1);
+      }
+    }
     // lane d: the warp's tokens that reach destination d (and d + 32)
     col_lo[r] = warp_transpose32(static_cast<uint32_t>(dmask[r]), lane);
     if (lane < R) wcnt[r * WARPS + warp][lane] = __popc(col_lo[r]);
@@ -537,16 +554,27 @@ __global__ void __launch_bounds__(kRowsThreads, 1) layout_rows_kernel(LayoutArgs
     in_d[c][d] = n;
     for (int q = c + 1; q < C; ++q) cluster.map_shared_rank(&in_d[0][0], q)[c * kMaxRanks + d] = n;
   }
-  for (int q = 0; q < C; ++q) {
-    int32_t* dst = (q == c ? in_e : cluster.map_shared_rank(in_e, q)) + c * EB;
-    for (int j = tid; j < EB; j += THREADS) {
-      const int x = q * EB + j;
-      if (x < E) dst[j] = cnt_e[x];
+  if constexpr (EXPAND) {
+    for (int x = tid; x < E; x += THREADS) {
+      int n = 0;
+#pragma unroll
+      for (int rw = 0; rw < RW; ++rw) n += __popc(ebits[rw * E + x]);
+      cnt_e[x] = n;
+      for (int q = c + 1; q < C; ++q) cluster.map_shared_rank(in_e, q)[c * E + x] = n;
+    }
+  } else {
+    for (int q = 0; q < C; ++q) {
+      int32_t* dst = (q == c ? in_e : cluster.map_shared_rank(in_e, q)) + c * EB;
+      for (int j = tid; j < EB; j += THREADS) {
+        const int x = q * EB + j;
+        if (x < E) dst[j] = cnt_e[x];
+      }
     }
   }
   cluster.sync();
 
-  // ---- bases: this CTA's (round, warp) counts become their first slots
+  // ---- bases: this CTA's (round, warp) counts become their first slots (and
+  // expanded, their first source-local positions)
   const int rb = row_block(s, a.n_so, a.n_su);
   for (int d = tid; d < R; d += THREADS) {
     int base = 0;
@@ -566,26 +594,42 @@ __global__ void __launch_bounds__(kRowsThreads, 1) layout_rows_kernel(LayoutArgs
       run += n;
     }
   }
-  // this CTA's share of the source's per-expert totals
-  for (int j = tid; j < EB; j += THREADS) {
-    const int x = c * EB + j;
-    if (x < E) {
-      int n = 0;
+  if constexpr (EXPAND) {
+    for (int x = tid; x < E; x += THREADS) {
+      int run = 0;
 #pragma unroll
       for (int q = 0; q < 8; ++q)
-        if (q < C) n += in_e[q * EB + j];
-      a.num_tokens_per_expert[s * E + x] = n;
+        if (q < c) run += in_e[q * E + x];
+      if (c == C - 1) a.num_tokens_per_expert[s * E + x] = run + cnt_e[x];
+#pragma unroll
+      for (int rw = 0; rw < RW; ++rw) {
+        ebase[rw * E + x] = run;
+        run += __popc(ebits[rw * E + x]);
+      }
+    }
+  } else {
+    // this CTA's share of the source's per-expert totals
+    for (int j = tid; j < EB; j += THREADS) {
+      const int x = c * EB + j;
+      if (x < E) {
+        int n = 0;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (q < C) n += in_e[q * EB + j];
+        a.num_tokens_per_expert[s * E + x] = n;
+      }
     }
   }
   __syncthreads();
   uint32_t arrived = 0;
   if (tid == 0) arrived = count_in(a);
 
-  // ---- pass 2: slots, no barriers
+  // ---- pass 2: slots (and source-local positions), no barriers
 #pragma unroll
   for (int r = 0; r < ROUNDS; ++r) {
     const int t = t_begin + r * THREADS + tid;
-    int slot[KMAX];
+    const int rw = r * WARPS + warp;
+    int slot[KMAX], pos[KMAX];
 #pragma unroll
     for (int k = 0; k < KMAX; ++k) {
       const int d = e[r][k] >= 0 ? div_l(e[r][k], a.l_magic) : 0;
@@ -595,22 +639,33 @@ __global__ void __launch_bounds__(kRowsThreads, 1) layout_rows_kernel(LayoutArgs
         if (d >= 32) col = hi;
       }
       slot[k] = -1;
+      pos[k] = -1;
       if (e[r][k] >= 0) {
-        slot[k] = wcnt[r * WARPS + warp][d] + __popc(col & lt);
+        slot[k] = wcnt[rw][d] + __popc(col & lt);
         // checked builds: the slot stays inside this source's row block
         if (!row_in_bounds(slot[k] - static_cast<int64_t>(rb) * a.M, a.M, a.err)) slot[k] = -1;
+        if constexpr (EXPAND) pos[k] = ebase[rw * E + e[r][k]] + __popc(ebits[rw * E + e[r][k]] & lt);
       }
     }
     if (t < t_end) {
       const int64_t tok = tok_base + t;
       int32_t* srow = a.slot_map + tok * a.K;
-      if (a.K == KMAX && aligned16(srow)) {
+      int32_t* prow = EXPAND ? a.exp_pos + tok * a.K : nullptr;
+      if (a.K == KMAX && aligned16(srow) && (!EXPAND || aligned16(prow))) {
         *reinterpret_cast<int4*>(srow) = make_int4(slot[0], slot[1], slot[2], slot[3]);
         *reinterpret_cast<int4*>(srow + 4) = make_int4(slot[4], slot[5], slot[6], slot[7]);
+        if constexpr (EXPAND) {
+          *reinterpret_cast<int4*>(prow) = make_int4(pos[0], pos[1], pos[2], pos[3]);
+          *reinterpret_cast<int4*>(prow + 4) = make_int4(pos[4], pos[5], pos[6], pos[7]);
+        }
       } else {
 #pragma unroll
-        for (int k = 0; k < KMAX; ++k)
-          if (k < a.K) srow[k] = slot[k];
+        for (int k = 0; k < KMAX; ++k) {
+          if (k < a.K) {
+            srow[k] = slot[k];
+            if constexpr (EXPAND) prow[k] = pos[k];
+          }
+        }
       }
       uint8_t* row = a.is_token_in_rank + tok * R;
       if ((R & 15) == 0 && aligned16(row)) {
@@ -767,6 +822,13 @@ cudaError_t launch_clusters(Kernel kernel, const Geometry& g, const LayoutArgs& 
   return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
+template <bool EXPAND>
+cudaError_t launch_rows(int rounds, const Geometry& g, const LayoutArgs& a, size_t smem, cudaStream_t stream) {
+  if (rounds <= 1) return launch_clusters(layout_rows_kernel<1, EXPAND>, g, a, kRowsThreads, smem, stream);
+  if (rounds <= 2) return launch_clusters(layout_rows_kernel<2, EXPAND>, g, a, kRowsThreads, smem, stream);
+  return launch_clusters(layout_rows_kernel<4, EXPAND>, g, a, kRowsThreads, smem, stream);
+}
+
 template <int KMAX, int THREADS>
 cudaError_t launch_main(const Geometry& g, const LayoutArgs& a, cudaStream_t stream) {
   const size_t smem = sizeof(int32_t) * g.E +
@@ -779,16 +841,15 @@ cudaError_t launch_main(const Geometry& g, const LayoutArgs& a, cudaStream_t str
 cudaError_t launch_layout(const Geometry& g, const LayoutArgs& args, int num_prologue_sms,
                           cudaStream_t stream) {
   LayoutArgs a = args;
-  // One thread per token and round. Row form with top-k <= 8: 256-thread CTAs,
-  // as many per source as make rounds of 256 tokens, at most 8 (a portable
-  // cluster; on GB300 a 16th cluster of 512-thread CTAs started about 7 us after
-  // the others), each holding up to four rounds in registers. Otherwise (the
-  // expanded layout, whose per-warp expert bitmaps take shared memory, or
-  // top-k above 8, whose lanes do not fit 512 threads' registers) 256-thread
-  // CTAs of the general kernel. Always within the prologue budget of 2 CTAs per
-  // requested SM, and at least one CTA per source.
-  const bool rows = !g.expand && g.K <= 8;
-  const int threads = rows ? kRowsThreads : 256;
+  // One thread per token and round in CTAs of 256 threads, as many per source
+  // as make rounds of 256 tokens, at most 8 (a portable cluster; on GB300 a
+  // 16th cluster of 512-thread CTAs started about 7 us after the others).
+  // Top-k <= 8 with at most four rounds a CTA runs the register kernel (the
+  // expanded layout too, while its per-(round, warp) expert tables fit in
+  // shared memory); otherwise the general kernel, which loads the rounds in
+  // turn. Always within the prologue budget of 2 CTAs per requested SM, and at
+  // least one CTA per source.
+  const int threads = kRowsThreads;
   const int sms = num_prologue_sms > 0 ? (num_prologue_sms < kMaxPrologueCtas ? num_prologue_sms
                                                                                : kMaxPrologueCtas)
                                        : kMaxPrologueCtas;
@@ -802,14 +863,22 @@ cudaError_t launch_layout(const Geometry& g, const LayoutArgs& args, int num_pro
   a.so_magic = g.n_so == 1 ? 0u : static_cast<uint32_t>((0x100000000ull + g.n_so - 1) / g.n_so);
   a.EB = (g.E + C - 1) / C;
   const int rounds = (a.TB + threads - 1) / threads;
-  const size_t smem_rows = sizeof(int32_t) * (g.E + static_cast<size_t>(C) * a.EB);
+  const int rt = rounds <= 1 ? 1 : (rounds <= 2 ? 2 : 4);  // the kernel's rounds
+  const size_t smem_rows =
+      sizeof(int32_t) * (g.expand ? static_cast<size_t>(g.E) * (1 + C + 2 * rt * (kRowsThreads / 32))
+                                  : g.E + static_cast<size_t>(C) * a.EB);
+  static int smem_optin = 0;
+  if (smem_optin == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      return cudaErrorUnknown;
+  }
+  // the register kernel's static shared memory stays under 12 KB
+  const bool rows = g.K <= 8 && rounds <= 4 && smem_rows + 12 * 1024 <= static_cast<size_t>(smem_optin);
   cudaError_t err;
-  if (rows && rounds <= 1)
-    err = launch_clusters(layout_rows_kernel<1>, g, a, threads, smem_rows, stream);
-  else if (rows && rounds <= 2)
-    err = launch_clusters(layout_rows_kernel<2>, g, a, threads, smem_rows, stream);
-  else if (rows && rounds <= 4)
-    err = launch_clusters(layout_rows_kernel<4>, g, a, threads, smem_rows, stream);
+  if (rows)
+    err = g.expand ? launch_rows<true>(rt, g, a, smem_rows, stream) : launch_rows<false>(rt, g, a, smem_rows, stream);
   else
     err = g.K <= 8 ? launch_main<8, 256>(g, a, stream) : launch_main<32, 256>(g, a, stream);
   if (err != cudaSuccess) return err;
