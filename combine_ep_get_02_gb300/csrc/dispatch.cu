@@ -54,19 +54,41 @@ __global__ void __launch_bounds__(kCopyThreads, kKind == kCastRow ? 2 : 4) dispa
     const RawLane cur = next;
     const int64_t after = take_unit(us, a.queue, lane);
     next = fetch_lane(a, us.nxt, lane, kExpand, kAtomic);
+    // the row's first loads go out before its destinations are resolved: its
+    // address depends on the token alone
+    const uint8_t* src = a.x + tok * a.in_row_bytes;
+    uint4 v[kKind == kCopyRow ? kUnroll : 2 * kCastUnits];
+    if (kKind == kCopyRow) {
+      const int nchunk = a.in_row_bytes >> 4;
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int c = u * 32 + lane;
+        if (c < nchunk) v[u] = ld_stream16(src + (static_cast<size_t>(c) << 4));
+      }
+    } else {
+      const int nunit = a.H >> 4;
+#pragma unroll
+      for (int r = 0; r < kCastUnits; ++r) {
+        const int u = r * 32 + lane;
+        if (u < nunit) {
+          v[2 * r] = ld_stream16(src + (static_cast<size_t>(u) << 5));
+          v[2 * r + 1] = ld_stream16(src + (static_cast<size_t>(u) << 5) + 16);
+        }
+      }
+    }
     const TokenLanes ln = lanes_of(a, cur, tok, lane, kExpand, kAtomic);
     const int nh = hidden_rows(a, ln, lane, kExpand, s_row[warp]);
 
     if (kKind == kCopyRow) {
       // the row's bytes unchanged (bf16 -> bf16, or pre-cast e4m3 -> e4m3)
-      const uint8_t* src = a.x + tok * a.in_row_bytes;
       const int nchunk = a.in_row_bytes >> 4;
       for (int c0 = 0; c0 < nchunk; c0 += 32 * kUnroll) {
-        uint4 v[kUnroll];
+        if (c0 > 0) {
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-          const int c = c0 + u * 32 + lane;
-          if (c < nchunk) v[u] = ld_stream16(src + (static_cast<size_t>(c) << 4));
+          for (int u = 0; u < kUnroll; ++u) {
+            const int c = c0 + u * 32 + lane;
+            if (c < nchunk) v[u] = ld_stream16(src + (static_cast<size_t>(c) << 4));
+          }
         }
         for (int j = 0; j < nh; ++j) {
           uint8_t* dst = a.recv_x + s_row[warp][j] * a.out_row_bytes;
@@ -87,23 +109,23 @@ __global__ void __launch_bounds__(kCopyThreads, kKind == kCastRow ? 2 : 4) dispa
     } else {
       // bf16 -> e4m3 with one fp32 scale per 128 columns. A lane owns 16 columns
       // (32 bytes in, 16 bytes out); 8 consecutive lanes form one 128-column group.
-      const uint8_t* src = a.x + tok * a.in_row_bytes;
       const int nunit = a.H >> 4;  // multiple of 8
       for (int u0 = 0; u0 < nunit; u0 += 32 * kCastUnits) {
-        uint4 lo[kCastUnits], hi[kCastUnits];
+        if (u0 > 0) {
 #pragma unroll
-        for (int r = 0; r < kCastUnits; ++r) {
-          const int u = u0 + r * 32 + lane;
-          if (u < nunit) {
-            lo[r] = ld_stream16(src + (static_cast<size_t>(u) << 5));
-            hi[r] = ld_stream16(src + (static_cast<size_t>(u) << 5) + 16);
+          for (int r = 0; r < kCastUnits; ++r) {
+            const int u = u0 + r * 32 + lane;
+            if (u < nunit) {
+              v[2 * r] = ld_stream16(src + (static_cast<size_t>(u) << 5));
+              v[2 * r + 1] = ld_stream16(src + (static_cast<size_t>(u) << 5) + 16);
+            }
           }
         }
 #pragma unroll
         for (int r = 0; r < kCastUnits; ++r) {
           const int u = u0 + r * 32 + lane;
           if (u0 + r * 32 >= nunit) continue;  // warp-uniform
-          const CastUnit cu = cast_unit(lo[r], hi[r], u < nunit, a.sf_pack);
+          const CastUnit cu = cast_unit(v[2 * r], v[2 * r + 1], u < nunit, a.sf_pack);
           const uint4 q = cu.q;
           if (u < nunit) {
             if ((lane & 7) == 0) {
