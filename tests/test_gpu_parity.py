@@ -54,6 +54,14 @@ EXTRA = {
                                     sf_pack=True),
     "max_hidden_precast_packed": W.Workload("max_hidden_precast_packed", 1, 4, 16, 4, 40, 40, 16384,
                                             x_dtype="fp8", recv_dtype="fp8", sf_pack=True),
+    # the general layout kernel with top-k <= 8: expanded with more experts than the register
+    # kernel's per-(round, warp) expert tables hold in shared memory, and more than four rounds
+    # of 256 tokens per CTA (row form and expanded)
+    "expand_many_experts": W.Workload("expand_many_experts", 1, 4, 4096, 8, 40, 40, 128, expand=True,
+                                      expert_alignment=2, routing="zipf", y_kind="random"),
+    "long_tokens": W.Workload("long_tokens", 1, 2, 16, 8, 8500, 8500, 64, mask_frac=0.05),
+    "long_tokens_expand": W.Workload("long_tokens_expand", 1, 2, 16, 4, 8500, 8500, 64, expand=True,
+                                     expert_alignment=4, zero_padding=True, y_kind="random"),
 }
 
 CASES = dict(W.PARITY)
