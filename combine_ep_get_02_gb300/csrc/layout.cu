@@ -17,9 +17,10 @@
 //   pass 2  warp prefix of the ballots plus the running base gives each lane's
 //           slot; the expanded layout ranks a lane among its expert's lanes with
 //           per-warp bitmaps of the tokens (source-local position).
-// layout_rows_kernel computes the same for the row form with top-k <= 8, with
-// every lane in registers and the counts pushed to the cluster peers instead of
-// read from them (its own comment below).
+// layout_rows_kernel computes the same for top-k <= 8 (row form, and the
+// expanded positions while their per-(round, warp) tables fit in shared
+// memory), with every lane in registers and the counts pushed to the cluster
+// peers instead of read from them (its own comment below).
 // The last CTA of the grid to finish (a counter in the workspace, no waiting)
 // turns the receive counts into their prefix sums, and the destinations'
 // totals into the first packed row of each destination.
