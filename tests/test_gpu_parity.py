@@ -62,6 +62,11 @@ EXTRA = {
     "long_tokens": W.Workload("long_tokens", 1, 2, 16, 8, 8500, 8500, 64, mask_frac=0.05),
     "long_tokens_expand": W.Workload("long_tokens_expand", 1, 2, 16, 4, 8500, 8500, 64, expand=True,
                                      expert_alignment=4, zero_padding=True, y_kind="random"),
+    # the register layout kernel with two and four rounds of 256 tokens per CTA (8 CTAs a source)
+    "rounds4_rows": W.Workload("rounds4_rows", 1, 2, 16, 8, 7000, 7000, 64, mask_frac=0.05),
+    "rounds2_expand": W.Workload("rounds2_expand", 1, 2, 16, 4, 3000, 3000, 64, expand=True, y_kind="random"),
+    "rounds4_expand": W.Workload("rounds4_expand", 1, 2, 32, 8, 7000, 7000, 64, expand=True,
+                                 expert_alignment=2, zero_padding=True, routing="zipf", y_kind="random"),
 }
 
 CASES = dict(W.PARITY)
