@@ -148,13 +148,11 @@ cudaError_t launch_dispatch_bulk(const Geometry& g, const DispatchArgs& a, int n
   // the launch may be placed while the kernel before it drains (see pdl_wait),
   // when SMs with free shared memory could otherwise take several CTAs each
   // and leave others without. So ask for more than half an SM's shared memory.
-  static int sm_smem = 0;
-  if (sm_smem == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess)
-      return cudaErrorUnknown;
-  }
+  int dev = 0, sm_smem = 0;
+  cudaError_t qerr;
+  if ((qerr = cudaGetDevice(&dev)) != cudaSuccess ||
+      (qerr = cudaDeviceGetAttribute(&sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess)
+    return qerr;
   const size_t half = static_cast<size_t>(sm_smem) / 2 + 1024;
   if (smem < half) smem = half;
   auto kern = g.expand ? dispatch_bulk_kernel<true> : dispatch_bulk_kernel<false>;

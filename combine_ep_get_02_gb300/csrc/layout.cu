@@ -868,13 +868,11 @@ cudaError_t launch_layout(const Geometry& g, const LayoutArgs& args, int num_pro
   const size_t smem_rows =
       sizeof(int32_t) * (g.expand ? static_cast<size_t>(g.E) * (1 + C + 2 * rt * (kRowsThreads / 32))
                                   : g.E + static_cast<size_t>(C) * a.EB);
-  static int smem_optin = 0;
-  if (smem_optin == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
-      return cudaErrorUnknown;
-  }
+  int dev = 0, smem_optin = 0;
+  cudaError_t qerr;
+  if ((qerr = cudaGetDevice(&dev)) != cudaSuccess ||
+      (qerr = cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
+    return qerr;
   // the register kernel's static shared memory stays under 12 KB
   const bool rows = g.K <= 8 && rounds <= 4 && smem_rows + 12 * 1024 <= static_cast<size_t>(smem_optin);
   cudaError_t err;
