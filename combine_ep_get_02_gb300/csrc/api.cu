@@ -305,7 +305,7 @@ int ep_dispatch(const ep_config_t* cfg, const ep_layout_t* layout, const void* x
   if (recv->recv_x_rows < need_rows) return EP_ERR_INVALID_ARG;
   const int sms = sms_or_all(cfg->num_sms);
   if (sms < 0) return EP_ERR_CUDA;
-  DispatchArgs a;
+  DispatchArgs a = {};
   a.x = static_cast<const uint8_t*>(x);
   a.x_sf = x_sf;
   a.topk_idx = topk_idx;

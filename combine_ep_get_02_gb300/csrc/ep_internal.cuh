@@ -133,6 +133,8 @@ struct DispatchArgs {
   int64_t region_rows;
   int64_t num_tokens;
   int in_row_bytes, out_row_bytes;
+  int splits;     // register-path work units per token (column ranges); 1 elsewhere
+  int split_len;  // 16-byte chunks (row copy) or 16-column units (cast) per range
 };
 
 // The post-hoc sort of the comparison path: permutes each (destination, row
