@@ -136,11 +136,14 @@ cudaError_t launch_one(const CombineArgs& args, int num_sms, cudaStream_t stream
   if (per_sm < 1) per_sm = 1;
   CombineArgs a = args;
   // Split tokens into column ranges until every warp gets about 16 units, so
-  // that the last wave is short; a range is a whole number of lane sweeps.
+  // that the last wave is short; a range is a whole number of lane sweeps, at
+  // least two (a one-sweep range pays its routing loads for too few bytes)
+  // unless two-sweep ranges would leave warps without a unit.
   const int64_t warps = static_cast<int64_t>(num_sms) * per_sm * kWarps;
   const int nchunk = a.H >> 3;
   const int sweep = 32 * kSteps;
-  const int max_splits = (nchunk + sweep - 1) / sweep;
+  int max_splits = (nchunk + 2 * sweep - 1) / (2 * sweep);
+  if (a.num_tokens * max_splits < warps) max_splits = (nchunk + sweep - 1) / sweep;
   int64_t want = a.num_tokens > 0 ? (16 * warps + a.num_tokens - 1) / a.num_tokens : 1;
   if (want > max_splits) want = max_splits;
   if (want < 1) want = 1;
